@@ -1,0 +1,505 @@
+"""Benchmark of the layer-wise paged KV block reshuffle on one GB300 (or N replicas).
+
+One step = the whole hot path over one batch: the batch plan, then for every layer
+slice (hit_layer[l]), merge-scatter (hit + miss into the paged pool), gather (pool ->
+per-layer K/V objects) and scatter-back (objects -> pool).  The ops run phase by
+phase (all layers of one op, then the next op), so no kernel finds its inputs in L2:
+every phase streams at least 8 GB through a 129 MB L2.
+
+Prints one JSON line.  `value` is algorithmic bytes moved (read + write, every op)
+per second of the timed region, in GB/s; `roofline` is the dominant kernel's
+achieved bandwidth against the measured HBM copy peak; `e2e` repeats the step with
+the inputs copied from pinned host memory and the objects read back inside the timed
+region; `cpu_baseline` is the CPU oracle on a bounded sample of the same workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference   # the CPU oracle on the host cores
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "KV reshuffle HBM GB/s (read+write) and % of GB300 peak; µs per layer"
+UNIT = "GB/s"
+DEFAULT_WORKLOAD = "llama3_8b_agentic"
+FALLBACK_HBM_GBS = 6800.0
+OPS = ("slice", "merge_scatter", "gather", "scatter_back")
+KERNEL_NAMES = {"slice": "kvl_slice_kernel", "merge_scatter": "kvl_merge_scatter_kernel",
+                "gather": "kvl_gather_kernel", "scatter_back": "kvl_scatter_back_kernel"}
+
+
+# ---------------------------------------------------------------------------
+# Bytes each op moves (algorithmic: each byte read once and written once)
+# ---------------------------------------------------------------------------
+
+def op_bytes(spec) -> dict:
+    """Algorithmic read+write bytes of one launch of each op (one layer, whole batch)."""
+    R = spec.R
+    hit = int(sum(spec.t_hit))
+    tokens = int(spec.t_all().sum())
+    blocks = int(spec.nblk().sum())
+    return {"slice": 2 * hit * R, "merge_scatter": 2 * tokens * R,
+            "gather": 2 * spec.P * blocks * spec.B * spec.Rp,
+            "scatter_back": 2 * spec.P * blocks * spec.B * spec.Rp}
+
+
+def step_bytes(spec) -> int:
+    return spec.L * sum(op_bytes(spec).values())
+
+
+def describe(spec) -> dict:
+    d = dict(workload=spec.name, L=spec.L, P=spec.P, B=spec.B, Rp=spec.Rp,
+             requests=spec.n_req, T_hit=int(sum(spec.t_hit)), T_miss=int(sum(spec.t_miss)),
+             pool_blocks=spec.n_pool, payload={"normal": "bf16 N(0,1)",
+                                                "uniform2": "bf16 U[-2,2]"}.get(spec.values, spec.values),
+             step="plan, then per layer slice, merge-scatter, gather, scatter-back "
+                  "(each op over all layers before the next op)",
+             l2="inputs larger than L2: every phase streams >= 8 GB past a 129 MB L2")
+    if spec.name == "llama3_8b_agentic":
+        d.update(H_kv=8, d=128)
+    return d
+
+
+# ---------------------------------------------------------------------------
+# Multi-rank plumbing (one process per GPU; replicas, no data-path collective)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """Largest value over all ranks (the slowest rank sets the job's time)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and str(device).startswith("cuda"):
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# Clocks during the timed region
+# ---------------------------------------------------------------------------
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int, path: Path | None):
+        self.proc, self.path, self.gpu = None, path, gpu_index
+
+    def __enter__(self):
+        try:
+            self.out = open(self.path, "w") if self.path else subprocess.PIPE
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out if self.path else subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is None:
+            self.text = ""
+            return False
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        if self.path:
+            self.out.close()
+            out = self.path.read_text()
+        self.text = out or ""
+        return False
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.text.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# Peaks and ncu traffic records
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    p = ROOT / "MEASURED_PEAKS.json"
+    try:
+        v = float(json.loads(p.read_text())["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted((ROOT / "layer_wise_paged_gb300" / "csrc").glob("*")):
+        h.update(f.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes from the committed ncu record, if it was taken on this
+    kernel source (else None)."""
+    p = ROOT / "profiles" / "traffic.json"
+    try:
+        rec = json.loads(p.read_text())
+    except (OSError, ValueError):
+        return None
+    for r in rec.get("records", []):
+        if r.get("kernel") == kernel and r.get("workload") == workload and \
+                r.get("source_sha") == kernel_source_hash():
+            return r.get("dram_bytes_per_launch")
+    return None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def _layer_shifted(requests, layer):
+    """Request layouts whose layer-0 view is `layer` of the original (pointer shift)."""
+    return [dataclasses.replace(q, hit_off=q.hit_off + layer * q.hit_layer_stride,
+                                miss_off=q.miss_off + layer * q.miss_layer_stride,
+                                obj_layer_stride=0) for q in requests]
+
+
+class OracleSample:
+    """Host buffers for the CPU oracle: the workload's full inputs, a one-layer pool
+    and one layer of objects; `run(layer)` does the step's four ops for that layer."""
+
+    def __init__(self, spec, hit=None, miss=None):
+        import torch
+        import oracle
+        self.spec = spec
+        lay = workloads.layout(spec, objects_one_layer=True)
+        self.lay = lay
+        if hit is None:
+            t = torch.empty(lay.hit_bytes, dtype=torch.uint8)
+            workloads.fill_payload(t, spec.values, spec.seed * 7 + 1)
+            hit = t.numpy()
+            t = torch.empty(max(16, lay.miss_bytes), dtype=torch.uint8)
+            workloads.fill_payload(t, spec.values, spec.seed * 7 + 2)
+            miss = t.numpy()
+        self.hit, self.miss = hit, miss
+        self.pool = np.full(spec.P * spec.n_pool * spec.B * spec.Rp, workloads.SENTINEL, np.uint8)
+        self.objects = np.full(max(16, lay.obj_bytes), workloads.SENTINEL, np.uint8)
+        self.tables = workloads.block_tables(spec)
+        self.src_tables = workloads.source_tables(spec)
+        self.g1 = dataclasses.replace(spec, L=1)
+        self.oracle = oracle
+
+    def run(self, layer: int) -> int:
+        ob = self.oracle.Batch(self.g1, _layer_shifted(self.lay.requests, layer), self.hit,
+                               self.miss, self.objects, self.tables, self.src_tables)
+        st, _ = ob.slice_layer(0)
+        s2, _ = ob.merge_scatter(0, self.pool)
+        s3 = ob.gather_objects(0, self.pool)
+        s4 = ob.scatter_back(0, self.pool)
+        if st or s2 or s3 or s4:
+            raise RuntimeError("oracle reported an error on the benchmark workload")
+        return sum(op_bytes(self.spec).values())
+
+
+def cpu_baseline(spec, budget_s=12.0, sample=None):
+    """Time the oracle layer by layer until `budget_s` is spent (at least one layer)."""
+    sample = sample or OracleSample(spec)
+    done_bytes, layers, t0 = 0, 0, time.perf_counter()
+    while layers < spec.L:
+        done_bytes += sample.run(layers)
+        layers += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(done_bytes / dt / 1e9, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{spec.name}: layers 0..{layers - 1} of {spec.L} (all four ops each), "
+                      f"{done_bytes / 1e9:.2f} GB algorithmic, {dt:.1f} s, single-threaded C"}
+
+
+def bench_spec(args):
+    """The named workload, or its first --layers layers (a smaller case of the same
+    kernels, for profiling captures that must fit in a few GB)."""
+    spec = workloads.get_spec(args.workload)
+    if args.layers:
+        spec = dataclasses.replace(spec, L=min(spec.L, args.layers))
+    return spec
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step one layer of the workload."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    spec = bench_spec(args)
+    sample = OracleSample(spec)
+    for s in range(args.warmup):
+        sample.run(s % spec.L)
+    t0 = time.perf_counter()
+    total = 0
+    for s in range(args.steps):
+        total += sample.run((args.warmup + s) % spec.L)
+    dt = time.perf_counter() - t0
+    v = total / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+            "config": describe(spec),
+            "cpu_baseline": {"value": round(v, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{spec.name}: one layer per step (all four ops), "
+                                       "single-threaded C oracle"},
+            "e2e": {"value": round(v, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# The GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args):
+    import torch
+    import layer_wise_paged_gb300 as kvl
+    from layer_wise_paged_gb300.batch import Batch
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the GPU arm has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    kvl.build()
+    kvl.lib()
+
+    spec = bench_spec(args)
+    bufs = workloads.allocate(spec, dev)
+    lay = bufs["layout"]
+    g = (spec.L, spec.P, spec.B, spec.Rp, spec.n_pool)
+    batch = Batch(g, lay.requests, bufs["hit"], bufs["miss"], bufs["objects"], bufs["tables"],
+                  bufs["src_tables"])
+    pool = bufs["pool"]
+    hit_out = torch.empty(max(16, spec.L * batch.total_hit * spec.R), dtype=torch.uint8, device=dev)
+    layer_hit = batch.total_hit * spec.R
+    hit_views = [hit_out[l * layer_hit:] for l in range(spec.L)]
+    stream = torch.cuda.current_stream(dev)
+    ev = {op: [] for op in OPS}
+
+    def step(record=False):
+        batch.plan(stream=stream)
+        phases = (
+            ("slice", lambda l: batch.slice_layer(l, hit_views[l], stream)),
+            ("merge_scatter", lambda l: batch.merge_scatter(l, pool, None, stream)),
+            ("gather", lambda l: batch.gather(l, pool, stream)),
+            ("scatter_back", lambda l: batch.scatter_back(l, pool, stream)),
+        )
+        for op, fn in phases:
+            for l in range(spec.L):
+                if record:
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    fn(l)
+                    b.record(stream)
+                    ev[op].append((a, b))
+                else:
+                    fn(l)
+
+    launches_per_step = kvl.kvl_launches_per_call(0) + spec.L * 4
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    code, detail = batch.status(stream)
+    if code != 0:
+        raise SystemExit(f"bench.py: plan status {code} detail {detail}")
+
+    clocks_path = ROOT / "gpurun_out" / "clocks.csv" if (ROOT / "gpurun_out").is_dir() else None
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local, clocks_path) as clk:
+        time.sleep(0.3)
+        t0.record(stream)
+        for _ in range(args.steps):
+            step(record=True)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    elapsed = t0.elapsed_time(t1) / 1e3
+    elapsed = max_over_ranks(elapsed, dist, dev)
+    code, detail = batch.status(stream)
+    if code != 0:
+        raise SystemExit(f"bench.py: status {code} detail {detail} after the timed steps")
+
+    sb = step_bytes(spec)
+    value = world * sb * args.steps / elapsed / 1e9
+    per_op = {}
+    for op in OPS:
+        ts = [a.elapsed_time(b) / 1e3 for a, b in ev[op]]
+        avg = sum(ts) / len(ts)
+        per_op[op] = {"us_per_launch": round(avg * 1e6, 2),
+                      "gbs": round(op_bytes(spec)[op] / avg / 1e9, 1),
+                      "total_s": sum(ts)}
+    dom = max(OPS, key=lambda o: per_op[o]["total_s"])
+    peak, peak_kind = hbm_peak()
+    achieved = per_op[dom]["gbs"]
+    traffic = recorded_traffic(KERNEL_NAMES[dom], spec.name)
+    roofline = {"bound": "hbm", "kernel": KERNEL_NAMES[dom] + f" ({dom})",
+                "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                "algorithmic_bytes_per_launch": op_bytes(spec)[dom],
+                "traffic": traffic}
+    kernels = {op: {k: v for k, v in per_op[op].items() if k != "total_s"} for op in OPS}
+
+    # ---- end to end: pinned host inputs in, objects out, inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        h_hit = torch.empty(bufs["hit"].numel(), dtype=torch.uint8, pin_memory=True)
+        h_miss = torch.empty(bufs["miss"].numel(), dtype=torch.uint8, pin_memory=True)
+        h_tab = torch.empty(bufs["tables"].numel(), dtype=torch.int32, pin_memory=True)
+        h_obj = torch.empty(bufs["objects"].numel(), dtype=torch.uint8, pin_memory=True)
+        h_hit.copy_(bufs["hit"])
+        h_miss.copy_(bufs["miss"])
+        h_tab.copy_(bufs["tables"])
+        h_in = h_hit.numel() + h_miss.numel() + 4 * h_tab.numel()
+        h_out = h_obj.numel()
+
+        def e2e_step():
+            bufs["hit"].copy_(h_hit, non_blocking=True)
+            bufs["miss"].copy_(h_miss, non_blocking=True)
+            bufs["tables"].copy_(h_tab, non_blocking=True)
+            step()
+            h_obj.copy_(bufs["objects"], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        n_e2e = max(3, min(args.e2e_steps, args.steps))
+        barrier(dist, dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        et = max_over_ranks(e0.elapsed_time(e1) / 1e3, dist, dev)
+        e2e = {"value": round(world * sb * n_e2e / et / 1e9, 2), "unit": UNIT,
+               "h2d_bytes_per_step": int(h_in), "d2h_bytes_per_step": int(h_out),
+               "steps": n_e2e, "ms_per_step": round(et / n_e2e * 1e3, 3),
+               "path": "pinned host -> device copies of the full block, miss KV and block "
+                       "tables; the step through the C ABI; objects -> pinned host"}
+        del h_hit, h_miss, h_tab, h_obj
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample = OracleSample(spec, hit=bufs["hit"].cpu().numpy(), miss=bufs["miss"].cpu().numpy())
+        cpu = cpu_baseline(spec, args.cpu_seconds, sample)
+        cpu["cores_available"] = os.cpu_count()
+
+    if rank == 0:
+        cfg = describe(spec)
+        cfg.update(us_per_layer=round(elapsed / args.steps / spec.L * 1e6, 2),
+                   step_bytes=sb, kernels=kernels, launches_per_step=launches_per_step,
+                   parallelism=f"{world} independent replica(s)", gpu=torch.cuda.get_device_name(dev))
+        line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(elapsed / args.steps * 1e3, 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+                "data": "synthetic (seeded bf16 KV payload; byte copies)", "config": cfg,
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches_per_step * args.steps * world,
+                "clocks": clk.summary()}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="kvl", choices=["kvl", "reference"])
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.NAMES)
+    p.add_argument("--layers", type=int, default=0,
+                   help="use only the first N layers of the workload (small profiling case)")
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    a = p.parse_args(argv)
+    if a.warmup < 3:
+        p.error("--warmup must be at least 3")
+    return a
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

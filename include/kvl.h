@@ -1,0 +1,198 @@
+/*
+ * kvl.h -- layer-wise paged KV block reshuffle on one GPU (GB300, sm_103a).
+ *
+ * C ABI of libkvl.so.  Every buffer is caller memory; the library allocates nothing,
+ * keeps no per-call state and never synchronises the caller's stream except in
+ * kvl_read_status.  All calls only ENQUEUE work on `stream` (a cudaStream_t passed as
+ * void*, NULL = the legacy default stream): results are valid once the caller has
+ * synchronised that stream or an event recorded after the call (DualPath KV Loading,
+ * "Dual-Path Loading", pe_read_path listing: every write is followed by a wait for
+ * its completion before the buffer is used).
+ *
+ * What the calls compute (the pages' objects, per layer l):
+ *   hit_full_block       persisted cross-layer KV of the hit prefix, semantic view
+ *                        [T_hit, L, C_KV]; here [T_hit, L, P, Rp] bytes, token-major
+ *                        (DualPath KV Loading, "Dual-Path Loading", objects table)
+ *   hit_layer[l]         = hit_full_block[:, l], [T_hit, P, Rp]          (slice_layer)
+ *   miss_layer[l]        freshly computed KV of the appended tokens, [T_miss, P, Rp]
+ *   complete_layer[l]    hit rows then miss rows, [T_all, P, Rp]   (concatenate_tokens)
+ *   paged pool           blocks of [B_tokens, H, d] linked per sequence by a block
+ *                        table (Tutti 阅读笔记, 前置知识 3 "分页 KV 内存管理", eq. (2))
+ *   K / V objects        one K and one V object per (layer, block): 2*L*ceil(T/B)
+ *                        objects per sequence (Tutti 阅读笔记, 前置知识 5, eqs. (3)(4);
+ *                        设计一 §3.1: one GPU file per block holding 2L objects)
+ *
+ * Geometry symbols: L layers, P planes per token (2 = K and V for head-split KV,
+ * 1 = one latent vector), B tokens per block, Rp bytes per token per plane
+ * (H_kv*d*2 for bf16 heads, C_KV*2 for a bf16 latent vector), R = P*Rp, N pool blocks.
+ * T_all = T_hit + T_miss, nblk = ceil(T_all / B), nsrc = ceil(T_hit / B).
+ *
+ * Layouts (byte addresses; every one is a plain byte copy, values never pass through
+ * arithmetic, so the results are bit-exact):
+ *   hit token t (t < T_hit), layer l, plane p:
+ *       hit_src + sb(t/B)*hit_block_stride + (t%B)*hit_token_stride
+ *               + l*hit_layer_stride + p*Rp,   sb(j) = hit_src_table ? hit_src_table[j] : j
+ *       (a contiguous full block [T_hit, L, P, Rp] has block stride B*L*R, token
+ *        stride L*R, layer stride R; a "Full Block" store of [B, L, P, Rp] blocks at
+ *        shuffled places uses hit_src_table)
+ *   miss token t (T_hit <= t < T_all):
+ *       miss_src + (t - T_hit)*miss_token_stride + l*miss_layer_stride + p*Rp
+ *   pool, block b, slot s:  pool + (((l*P + p)*N + b)*B + s)*Rp   ([L][P][N][B][Rp])
+ *   object (l, p, j) of a request, B*Rp bytes:
+ *       objects + l*obj_layer_stride + (p*nblk + j)*B*Rp
+ *       (obj_layer_stride = P*nblk*B*Rp gives [L][P][nblk][B][Rp], object id
+ *        (l*P + p)*nblk + j)
+ *   hit_out / complete_out: request r's token t at row hit_off[r] + t / tok_off[r] + t
+ *       of R bytes ([sum T_hit][P][Rp] / [sum T_all][P][Rp], requests in order)
+ *   block tables: one int32 array, request r's nblk entries at blk_off[r] (requests
+ *       packed back to back in order); one table serves every layer and plane.
+ *
+ * Partial blocks: the scatter writes only slots t < T_all; later slots of the last
+ * block keep their bytes.  Objects always carry whole blocks (fixed object size
+ * B*Rp), so a partial block's object carries whatever those slots hold.
+ *
+ * Alignment: Rp, every stride and every buffer address must be multiples of 16 bytes.
+ * Aliasing: sources, pool, objects and outputs must not overlap (undefined otherwise);
+ * with an injective block table every destination byte has exactly one writer.
+ *
+ * A plan records the request array and block tables it was built from; a call that
+ * passes other arrays with that plan is refused on the device (KVL_EINVAL).
+ *
+ * Errors: problems the host can see (null or misaligned arguments, a bad geometry,
+ * a layer outside [0, L), a plan too small) are returned at once and nothing is
+ * launched.  Problems only the device can see (negative counts, misaligned request
+ * fields, block ids out of range, duplicate block ids) are recorded in the plan's
+ * status word: the offending work is skipped, nothing traps, and every later call
+ * made with that plan does nothing until the plan is rebuilt.  kvl_read_status reads
+ * the word back.  KVL_ECUDA reports a failed launch.
+ */
+#ifndef KVL_H
+#define KVL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t kvl_status;
+
+#define KVL_OK 0
+#define KVL_EINVAL 1 /* bad argument or geometry, negative count, null pointer */
+#define KVL_EALIGN 2 /* pointer, stride or Rp not a multiple of 16 bytes */
+#define KVL_ERANGE 3 /* block id outside the pool / source, or plan capacity exceeded */
+#define KVL_EDUP 4   /* a pool block id used twice (only with check_injective) */
+#define KVL_ECUDA 5  /* a CUDA launch or copy failed */
+
+#define KVL_GATHER 0      /* kvl_gather_layer_objects: pool -> objects */
+#define KVL_SCATTER_BACK 1 /* kvl_gather_layer_objects: objects -> pool */
+
+/* Geometry shared by every request of a batch (host memory). */
+typedef struct kvl_geom {
+    int32_t n_layers;        /* L */
+    int32_t n_planes;        /* P: 2 = K,V planes; 1 = latent vector */
+    int32_t block_tokens;    /* B: tokens per paged block */
+    int32_t plane_row_bytes; /* Rp: bytes per token per plane, multiple of 16 */
+    int64_t pool_blocks;     /* N: physical blocks in the pool */
+} kvl_geom;
+
+/* One request (device memory: the calls take an array of these in device memory).
+ * All strides are in bytes. */
+typedef struct kvl_request {
+    const void *hit_src;          /* full block of the hit prefix (NULL if t_hit == 0) */
+    const int32_t *hit_src_table; /* NULL, or nsrc full-block ids (device memory) */
+    int64_t hit_src_blocks;       /* full blocks present at hit_src (bounds the ids) */
+    int64_t hit_block_stride;
+    int64_t hit_token_stride;
+    int64_t hit_layer_stride;
+    const void *miss_src;         /* miss KV (NULL if t_miss == 0) */
+    int64_t miss_token_stride;
+    int64_t miss_layer_stride;
+    void *objects;                /* this request's K/V objects (NULL if never gathered) */
+    int64_t obj_layer_stride;
+    int32_t t_hit;
+    int32_t t_miss;
+} kvl_request;
+
+/* Bytes of device memory a plan for n_req requests over a pool of pool_blocks needs.
+ * The plan holds at most pool_blocks work items: injective tables never need more. */
+size_t kvl_plan_bytes(int32_t n_req, int64_t pool_blocks);
+
+/* Plan layout, for callers that read the plan's arrays (byte offsets into the plan):
+ * off[0] header, off[1] tok_off (int64[n_req+1]), off[2] hit_off (int64[n_req+1]),
+ * off[3] blk_off (int64[n_req+1]), off[4] item_req (int32[pool_blocks]),
+ * off[5] item_blk (int32[pool_blocks]), off[6] injectivity bitmap, off[7] total bytes.
+ * The header's first int32 is the status and its int64 at byte 16 the item count. */
+void kvl_plan_layout(int32_t n_req, int64_t pool_blocks, size_t off[8]);
+
+/* kvl_batch_plan -- the batch's work list, built on the device.
+ * Computes exclusive prefix sums over requests of T_all (tok_off), T_hit (hit_off)
+ * and nblk (blk_off), and the work list item i = blk_off[r] + j -> (r, j) for every
+ * logical block j < nblk(r): the per-(request, block) items every later call walks,
+ * so one launch per layer covers the whole batch (Tutti 阅读笔记, 伪代码 1
+ * retrieve_layer and the note after it: the CPU launches the I/O kernel once per
+ * layer, O(L) not O(L x blocks)).  Validates each request (counts >= 0, required
+ * pointers non-null, 16-byte alignment), every pool block id (in [0, N)), every
+ * full-block id of a hit block (in [0, hit_src_blocks)) and, if check_injective,
+ * that no pool block id repeats.
+ *   geom            host pointer
+ *   d_reqs          device array of n_req requests (caller-owned, read only)
+ *   d_block_tables  device int32 tables, packed in request order (read only)
+ *   d_plan          device buffer of plan_bytes >= kvl_plan_bytes(n_req, N) bytes,
+ *                   16-byte aligned, caller-owned; overwritten
+ * Device-side status: EINVAL (detail = first bad request), EALIGN (detail = first bad
+ * request), ERANGE (detail = smallest bad work item, or the item count when it
+ * exceeds N), EDUP (detail = smallest repeated block id).  The largest code wins. */
+kvl_status kvl_batch_plan(const kvl_geom *geom, int32_t n_req, const kvl_request *d_reqs,
+                          const int32_t *d_block_tables, int32_t check_injective,
+                          void *d_plan, size_t plan_bytes, void *stream);
+
+/* kvl_slice_layer -- hit_layer[l] = hit_full_block[:, l] for every request
+ * (DualPath KV Loading, "Dual-Path Loading": objects table and the slice_layer step
+ * of pe_read_path / de_read_path).  Writes sum(T_hit) rows of R bytes to d_hit_out
+ * (device, caller-owned, request r's rows from hit_off[r]). */
+kvl_status kvl_slice_layer(const kvl_geom *geom, const void *d_plan, const kvl_request *d_reqs,
+                           int32_t layer, void *d_hit_out, void *stream);
+
+/* kvl_merge_scatter_paged -- slice, concatenate and scatter one layer in one pass:
+ * complete_layer[l] = hit_layer[l] rows then miss_layer[l] rows (DualPath KV Loading,
+ * pe_read_path concatenate_tokens; de_read_path merge_layer), and token t of plane p
+ * goes to pool block table[t / B], slot t % B (Tutti 阅读笔记, 前置知识 3, eq. (2)).
+ *   d_pool          device pool [L][P][N][B][Rp], caller-owned; slots of this layer
+ *                   named by the tables are written
+ *   d_complete_out  NULL, or device [sum T_all][P][Rp] that also receives
+ *                   complete_layer[l] (request r's rows from tok_off[r]) */
+kvl_status kvl_merge_scatter_paged(const kvl_geom *geom, const void *d_plan,
+                                   const kvl_request *d_reqs, const int32_t *d_block_tables,
+                                   int32_t layer, void *d_pool, void *d_complete_out,
+                                   void *stream);
+
+/* kvl_gather_layer_objects -- per-layer K/V objects <-> paged blocks.
+ * direction KVL_GATHER: object (l, p, j) = pool block table[j] of plane p, layer l,
+ * for every request: the 2*nblk objects of one layer ready for transfer (Tutti
+ * 阅读笔记, 前置知识 5 eq. (4); the worked trace's 8,000 per-layer entries for 4,000
+ * blocks).  direction KVL_SCATTER_BACK: the inverse, restoring objects into their
+ * paged blocks (伪代码 1 retrieve_layer).  Each request's `objects` must be non-NULL. */
+kvl_status kvl_gather_layer_objects(const kvl_geom *geom, const void *d_plan,
+                                    const kvl_request *d_reqs, const int32_t *d_block_tables,
+                                    int32_t layer, void *d_pool, int32_t direction,
+                                    void *stream);
+
+/* kvl_read_status -- copy the plan's status word and its detail to the host.
+ * Synchronises `stream` first, so it reports every call enqueued before it.
+ * code/detail may be NULL.  Returns KVL_ECUDA if the copy fails, else KVL_OK. */
+kvl_status kvl_read_status(const void *d_plan, int32_t *code, int64_t *detail, void *stream);
+
+/* Human-readable name of a status code (static string). */
+const char *kvl_status_string(kvl_status s);
+
+/* Kernel launches one call of each entry point makes (for launch accounting):
+ * which = 0 plan, 1 slice, 2 merge-scatter, 3 gather / scatter-back. */
+int32_t kvl_launches_per_call(int32_t which);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVL_H */

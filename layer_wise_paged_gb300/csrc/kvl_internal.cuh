@@ -1,0 +1,135 @@
+// kvl_internal.cuh -- internals shared by the plan and copy translation units of
+// libkvl.so: the plan's device layout, status recording, and host-side checks.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kvl.h"
+
+namespace kvl {
+
+constexpr uint32_t kPlanMagic = 0x4b564c31u;  // "KVL1"
+constexpr int kMaxDevices = 64;
+
+// Start of a plan (the header section is padded to 256 bytes).
+struct PlanHeader {
+    int32_t status;              // 0: KVL_* code, the largest recorded wins
+    uint32_t magic;              // 4: kPlanMagic once built
+    int32_t n_req;               // 8
+    int32_t check_injective;     // 12
+    int64_t n_items;             // 16: sum over requests of ceil(T_all / B)
+    int64_t n_tokens;            // 24: sum of T_all
+    int64_t n_hit;               // 32: sum of T_hit
+    int32_t scan_status;         // 40: status after the request scan (the fill reads it)
+    int32_t reserved;            // 44
+    int64_t pool_blocks;         // 48: N the plan was built for
+    int64_t block_tokens;        // 56: B the plan was built for
+    unsigned long long detail[8];  // 64: per status code, smallest detail recorded
+    const void *reqs;            // 128: the request array the plan was built from
+    const void *tables;          // 136: the block tables the plan was built from
+};
+static_assert(sizeof(PlanHeader) == 144, "plan header layout");
+static_assert(sizeof(kvl_request) == 96, "kvl_request layout");
+
+__host__ __device__ inline size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Byte offsets of the plan's sections (see kvl_plan_layout).
+struct PlanLayout {
+    size_t off[8];
+    __host__ __device__ PlanLayout() {}
+};
+
+__host__ __device__ inline PlanLayout plan_layout(int32_t n_req, int64_t pool_blocks)
+{
+    PlanLayout p;
+    size_t n1 = size_t(n_req < 0 ? 0 : n_req) + 1;
+    size_t cap = size_t(pool_blocks < 0 ? 0 : pool_blocks);
+    p.off[0] = 0;
+    p.off[1] = 256;
+    p.off[2] = p.off[1] + round256(n1 * 8);
+    p.off[3] = p.off[2] + round256(n1 * 8);
+    p.off[4] = p.off[3] + round256(n1 * 8);
+    p.off[5] = p.off[4] + round256(cap * 4);
+    p.off[6] = p.off[5] + round256(cap * 4);
+    p.off[7] = p.off[6] + round256(((cap + 31) / 32) * 4);
+    return p;
+}
+
+// Device view of a built plan.
+struct PlanView {
+    PlanHeader *hdr;
+    int64_t *tok_off;
+    int64_t *hit_off;
+    int64_t *blk_off;
+    int32_t *item_req;
+    int32_t *item_blk;
+    uint32_t *bitmap;
+};
+
+__host__ __device__ inline PlanView plan_view(void *d_plan, int32_t n_req, int64_t pool_blocks)
+{
+    PlanLayout l = plan_layout(n_req, pool_blocks);
+    char *b = static_cast<char *>(d_plan);
+    PlanView v;
+    v.hdr = reinterpret_cast<PlanHeader *>(b);
+    v.tok_off = reinterpret_cast<int64_t *>(b + l.off[1]);
+    v.hit_off = reinterpret_cast<int64_t *>(b + l.off[2]);
+    v.blk_off = reinterpret_cast<int64_t *>(b + l.off[3]);
+    v.item_req = reinterpret_cast<int32_t *>(b + l.off[4]);
+    v.item_blk = reinterpret_cast<int32_t *>(b + l.off[5]);
+    v.bitmap = reinterpret_cast<uint32_t *>(b + l.off[6]);
+    return v;
+}
+
+// Record a device-side error: the largest code wins, and each code keeps the
+// smallest detail it was given.
+__device__ __forceinline__ void record_error(PlanHeader *h, int code, unsigned long long detail)
+{
+    atomicMax(&h->status, code);
+    atomicMin(&h->detail[code], detail);
+}
+
+__host__ __device__ __forceinline__ bool aligned16(const void *p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+__host__ __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b)
+{
+    return (a + b - 1) / b;
+}
+
+// Host-side geometry check shared by every entry point.
+inline kvl_status check_geom(const kvl_geom *g)
+{
+    if (!g) return KVL_EINVAL;
+    if (g->n_layers <= 0 || g->n_planes <= 0 || g->block_tokens <= 0 ||
+        g->plane_row_bytes <= 0 || g->pool_blocks <= 0)
+        return KVL_EINVAL;
+    if (g->pool_blocks > INT32_MAX) return KVL_EINVAL;  // block ids are int32
+    if (g->plane_row_bytes % 16) return KVL_EALIGN;
+    return KVL_OK;
+}
+
+// SM count of the current device (cached per device).
+inline int sm_count()
+{
+    static int cache[kMaxDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev < 0 || dev >= kMaxDevices) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+inline kvl_status launch_status()
+{
+    return cudaGetLastError() == cudaSuccess ? KVL_OK : KVL_ECUDA;
+}
+
+}  // namespace kvl

@@ -1,0 +1,115 @@
+"""The C ABI without a GPU: the library builds, loads and exports every entry point
+include/kvl.h declares; the binding's structs match the header's; host-side
+argument checks answer before anything touches the device."""
+from __future__ import annotations
+
+import ctypes
+import re
+import subprocess
+from pathlib import Path
+
+import numpy as np
+import pytest
+
+import layer_wise_paged_gb300 as kvl
+
+ROOT = Path(__file__).resolve().parent.parent
+HEADER = ROOT / "include" / "kvl.h"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kvl.build()
+    return kvl.lib()
+
+
+def declared_functions():
+    text = re.sub(r"/\*.*?\*/", "", HEADER.read_text(), flags=re.S)
+    return sorted(set(re.findall(r"\b(kvl_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    out = subprocess.run(["nm", "-D", "--defined-only", str(kvl.LIB)], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r" T (kvl_\w+)", out))
+    for n in names:
+        assert n in exported, n
+        assert hasattr(lib, n)
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    prog = tmp_path / "layout.c"
+    fields = [f for f in kvl.REQUEST_DTYPE.names]
+    body = "\n".join(f'printf("{f} %zu\\n", offsetof(kvl_request, {f}));' for f in fields)
+    prog.write_text(f"""
+#include <stdio.h>
+#include <stddef.h>
+#include "kvl.h"
+int main(void) {{
+  printf("sizeof_request %zu\\n", sizeof(kvl_request));
+  printf("sizeof_geom %zu\\n", sizeof(kvl_geom));
+  printf("geom_pool_blocks %zu\\n", offsetof(kvl_geom, pool_blocks));
+  {body}
+  return 0;
+}}""")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-I", str(ROOT / "include"), str(prog), "-o", str(exe)],
+                   check=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True,
+                                                          text=True, check=True).stdout.splitlines())
+    assert int(got["sizeof_request"]) == kvl.REQUEST_DTYPE.itemsize == 96
+    assert int(got["sizeof_geom"]) == ctypes.sizeof(kvl.kvl_geom)
+    assert int(got["geom_pool_blocks"]) == kvl.kvl_geom.pool_blocks.offset
+    for f in fields:
+        assert int(got[f]) == kvl.REQUEST_DTYPE.fields[f][1], f
+
+
+def test_plan_layout_is_consistent(lib):
+    for n, N in [(0, 1), (1, 32), (16, 10625), (256, 49262), (1000, 1 << 20)]:
+        off = kvl.kvl_plan_layout(n, N)
+        assert off[0] == 0 and off[1] == 256
+        assert all(o % 256 == 0 for o in off)
+        assert off[2] - off[1] >= 8 * (n + 1) and off[4] - off[3] >= 8 * (n + 1)
+        assert off[5] - off[4] >= 4 * N and off[6] - off[5] >= 4 * N
+        assert off[7] - off[6] >= 4 * ((N + 31) // 32)
+        assert kvl.kvl_plan_bytes(n, N) == off[7]
+
+
+def test_status_strings_and_launch_counts(lib):
+    for c in range(6):
+        assert kvl.kvl_status_string(c)
+    assert kvl.kvl_launches_per_call(0) == 2
+    assert [kvl.kvl_launches_per_call(w) for w in (1, 2, 3)] == [1, 1, 1]
+
+
+def test_host_checks_answer_before_any_device_work(lib):
+    good = kvl.geom(2, 2, 16, 256, 64)
+    fake = 1 << 20  # never dereferenced: every call below fails its host checks first
+    assert kvl.kvl_batch_plan(kvl.geom(0, 2, 16, 256, 64), 1, fake, fake, 1, fake, 1 << 20) == kvl.KVL_EINVAL
+    assert kvl.kvl_batch_plan(kvl.geom(2, 2, 16, 24, 64), 1, fake, fake, 1, fake, 1 << 20) == kvl.KVL_EALIGN
+    assert kvl.kvl_batch_plan(good, 1, fake, fake, 1, 0, 1 << 20) == kvl.KVL_EINVAL
+    assert kvl.kvl_batch_plan(good, 1, fake, fake, 1, fake + 8, 1 << 20) == kvl.KVL_EALIGN
+    assert kvl.kvl_batch_plan(good, 1, fake, fake, 1, fake, 16) == kvl.KVL_EINVAL
+    assert kvl.kvl_batch_plan(good, -1, fake, fake, 1, fake, 1 << 20) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(good, fake, fake, fake, 2, fake) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(good, fake, fake, fake, 0, fake + 4) == kvl.KVL_EALIGN
+    assert kvl.kvl_gather_layer_objects(good, fake, fake, fake, 0, fake, 7) == kvl.KVL_EINVAL
+    assert kvl.kvl_slice_layer(good, fake, fake, 0, 0) == kvl.KVL_EINVAL
+    assert kvl.lib().kvl_read_status(None, None, None, None) == kvl.KVL_EINVAL
+
+
+def test_request_packing_follows_layouts():
+    import workloads
+    spec = workloads.custom_spec(L=3, P=2, B=4, Rp=32, t_hit=[10, 0], t_miss=[3, 5],
+                                 source="permuted")
+    lay = workloads.layout(spec)
+    arr = kvl.pack_requests(lay.requests, hit_base=1 << 32, miss_base=2 << 32,
+                            obj_base=3 << 32, src_table_base=4 << 32)
+    assert arr.shape == (2,)
+    assert arr[0]["hit_src"] == (1 << 32) + lay.requests[0].hit_off
+    assert arr[1]["hit_src"] == 0  # no hit tokens -> NULL
+    assert arr[0]["hit_src_table"] == (4 << 32)
+    assert arr[1]["miss_src"] == (2 << 32) + lay.requests[1].miss_off
+    assert arr[1]["t_miss"] == 5 and arr[0]["t_hit"] == 10

@@ -1,0 +1,153 @@
+"""Error paths on the GPU: every failure is a status code, never a fault.
+
+Host-visible problems return at once and launch nothing; device-visible ones are
+recorded in the plan's status word (compared with the oracle's verdict for the same
+planted error), the offending work is skipped, and later calls on a failed plan
+leave every buffer untouched.  Every planted error here keeps all accesses in bounds.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import layer_wise_paged_gb300 as kvl
+import oracle
+import workloads
+from tests._device import device_batch, to_dev
+from tests._host import geom_of, host_buffers
+
+pytestmark = pytest.mark.gpu
+
+SPEC = workloads.custom_spec(L=2, P=2, B=4, Rp=32, t_hit=[10, 0, 7, 8], t_miss=[3, 5, 0, 1],
+                             table="perm", source="permuted", seed=11)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    kvl.build()
+    kvl.lib()
+
+
+def _both(hb, requests=None, check_injective=True):
+    reqs = requests if requests is not None else hb.layout.requests
+    hb.layout.requests = reqs
+    gb, d = device_batch(SPEC, hb)
+    gb.plan(check_injective=check_injective)
+    ob = oracle.Batch(geom_of(SPEC), reqs, hb.hit, hb.miss, hb.objects, hb.tables, hb.src_tables)
+    op = ob.plan(check_injective=check_injective)
+    return gb, d, op
+
+
+@pytest.mark.parametrize("kind", ["pool_range", "dup", "dup_and_range", "src_range", "neg"])
+def test_plan_status_matches_oracle(kind):
+    hb = host_buffers(SPEC)
+    reqs = list(hb.layout.requests)
+    if kind == "pool_range":
+        hb.tables = hb.tables.copy(); hb.tables[9] = SPEC.n_pool; hb.tables[5] = -3
+    elif kind == "dup":
+        hb.tables = hb.tables.copy(); hb.tables[7] = hb.tables[2]
+    elif kind == "dup_and_range":
+        hb.tables = hb.tables.copy(); hb.tables[7] = hb.tables[2]; hb.tables[1] = 1 << 30
+    elif kind == "src_range":
+        hb.src_tables = hb.src_tables.copy(); hb.src_tables[4] = 99
+    elif kind == "neg":
+        reqs[3] = dataclasses.replace(reqs[3], t_hit=-2)
+    gb, d, op = _both(hb, reqs)
+    code, detail = gb.status()
+    assert code != 0
+    assert (code, detail) == (op["status"], op["detail"])
+    # a failed plan makes every later call a no-op
+    pool0 = d.pool.clone()
+    objs0 = d.objects.clone()
+    for layer in range(SPEC.L):
+        gb.merge_scatter(layer, d.pool)
+        gb.gather(layer, d.pool)
+    assert torch.equal(d.pool, pool0) and torch.equal(d.objects, objs0)
+    assert gb.status() == (code, detail)
+
+
+def test_duplicates_pass_without_the_check():
+    hb = host_buffers(SPEC)
+    hb.tables = hb.tables.copy(); hb.tables[7] = hb.tables[2]
+    gb, d, op = _both(hb, check_injective=False)
+    assert gb.status() == (0, 0) and op["status"] == 0
+
+
+def test_misaligned_request_fields_are_ealign():
+    hb = host_buffers(SPEC)
+    gb, d = device_batch(SPEC, hb)
+    host = kvl.pack_requests(hb.layout.requests, hit_base=d.hit.data_ptr(),
+                             miss_base=d.miss.data_ptr(), obj_base=d.objects.data_ptr(),
+                             src_table_base=d.src_tables.data_ptr())
+    for field, delta, want in [("hit_src", 8, kvl.KVL_EALIGN), ("miss_token_stride", 4, kvl.KVL_EALIGN),
+                               ("objects", 4, kvl.KVL_EALIGN)]:
+        bad = host.copy()
+        r = 0 if field != "miss_token_stride" else 1
+        bad[r][field] = int(bad[r][field]) + delta
+        gb.d_reqs.copy_(torch.from_numpy(bad.view(np.uint8).reshape(-1).copy()))
+        gb.plan()
+        assert gb.status() == (want, r), field
+        pool0 = d.pool.clone()
+        gb.merge_scatter(0, d.pool)
+        assert torch.equal(d.pool, pool0)
+
+
+def test_null_sources_are_einval():
+    hb = host_buffers(SPEC)
+    gb, d = device_batch(SPEC, hb)
+    host = kvl.pack_requests(hb.layout.requests, hit_base=0, miss_base=d.miss.data_ptr(),
+                             obj_base=d.objects.data_ptr(), src_table_base=d.src_tables.data_ptr())
+    gb.d_reqs.copy_(torch.from_numpy(host.view(np.uint8).reshape(-1).copy()))
+    gb.plan()
+    assert gb.status() == (kvl.KVL_EINVAL, 0)
+
+
+def test_tables_changed_after_planning_are_caught_by_the_copy_kernels():
+    hb = host_buffers(SPEC)
+    gb, d = device_batch(SPEC, hb)
+    gb.plan()
+    assert gb.status() == (0, 0)
+    d.tables[6] = SPEC.n_pool + 1
+    gb.merge_scatter(0, d.pool)
+    assert gb.status() == (kvl.KVL_ERANGE, 6)
+
+
+def test_missing_objects_pointer_is_einval_at_gather():
+    hb = host_buffers(SPEC)
+    gb, d = device_batch(SPEC, hb)
+    host = kvl.pack_requests(hb.layout.requests, hit_base=d.hit.data_ptr(),
+                             miss_base=d.miss.data_ptr(), obj_base=0,
+                             src_table_base=d.src_tables.data_ptr())
+    gb.d_reqs.copy_(torch.from_numpy(host.view(np.uint8).reshape(-1).copy()))
+    gb.plan()
+    gb.merge_scatter(0, d.pool)
+    assert gb.status() == (0, 0)
+    gb.gather(0, d.pool)
+    assert gb.status() == (kvl.KVL_EINVAL, 0)
+
+
+def test_host_side_checks_return_without_launching():
+    hb = host_buffers(SPEC)
+    gb, d = device_batch(SPEC, hb)
+    gb.plan()
+    g, plan, reqs, tabs = gb.g, gb.d_plan.data_ptr(), gb.d_reqs.data_ptr(), gb.tables.data_ptr()
+    pool = d.pool.data_ptr()
+    s = torch.cuda.current_stream().cuda_stream
+    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, SPEC.L, pool, None, s) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, -1, pool, None, s) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, pool + 8, None, s) == kvl.KVL_EALIGN
+    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 0, None, s) == kvl.KVL_EINVAL
+    assert kvl.kvl_gather_layer_objects(g, plan, reqs, tabs, 0, pool, 2, s) == kvl.KVL_EINVAL
+    assert kvl.kvl_slice_layer(g, plan, reqs, 0, 0, s) == kvl.KVL_EINVAL
+    assert kvl.kvl_batch_plan(g, gb.n_req, reqs, tabs, 1, plan, gb.plan_bytes - 1, s) == kvl.KVL_EINVAL
+    bad = kvl.geom(SPEC.L, SPEC.P, SPEC.B, 24, SPEC.n_pool)
+    assert kvl.kvl_merge_scatter_paged(bad, plan, reqs, tabs, 0, pool, None, s) == kvl.KVL_EALIGN
+    # a plan built for another pool size is refused on the device
+    other = kvl.geom(SPEC.L, SPEC.P, SPEC.B, SPEC.Rp, SPEC.n_pool - 1)
+    assert kvl.kvl_merge_scatter_paged(other, plan, reqs, tabs, 0, pool, None, s) == kvl.KVL_OK
+    assert gb.status()[0] == kvl.KVL_EINVAL

@@ -1,0 +1,215 @@
+"""GPU parity: every kernel, through the C ABI, byte for byte against the CPU oracle.
+
+Small cases (ragged batches that span many work items, mid-block hit/miss
+boundaries, partial last blocks, permuted sources, both miss layouts, one and two
+planes, row sizes from 16 B to 4 KiB, blocks of 1 to 64 tokens) compare whole
+buffers, guard bytes included.  The full-size workloads run in the benchmark's
+launch configuration and are compared with the oracle on sampled layers, with the
+scatter-back round trip checked on every layer.
+"""
+from __future__ import annotations
+
+from types import SimpleNamespace
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests._device import device_batch, one_layer_problem, sentinel_dev
+from tests._host import GUARD, geom_of, host_buffers
+
+pytestmark = pytest.mark.gpu
+
+SENT = workloads.SENTINEL
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import layer_wise_paged_gb300 as kvl
+    kvl.build()
+    kvl.lib()
+
+
+def oracle_batch(spec, hb):
+    return oracle.Batch(geom_of(spec), hb.layout.requests, hb.hit, hb.miss, hb.objects,
+                        hb.tables, hb.src_tables)
+
+
+def assert_bytes_equal(got_t, want, what):
+    got = got_t.cpu().numpy()
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    if not np.array_equal(got, want):
+        bad = np.nonzero(got != want)[0]
+        raise AssertionError(f"{what}: {bad.size} bytes differ, first at {bad[0]}")
+
+
+def run_parity(spec, *, check_injective=True, objects_one_layer=False, payload="bytes"):
+    hb = host_buffers(spec, objects_one_layer=objects_one_layer)
+    if payload == "spec":
+        # the workload's own value distribution, made once on the CPU
+        cpu = workloads.allocate(spec, "cpu", objects_one_layer=objects_one_layer)
+        hb.hit[:cpu["hit"].numel()] = cpu["hit"].numpy()[:hb.hit.size]
+        hb.miss[:cpu["miss"].numel()] = cpu["miss"].numpy()[:hb.miss.size]
+    gb, d = device_batch(spec, hb)
+    ob = oracle_batch(spec, hb)
+
+    gb.plan(check_injective=check_injective)
+    op = ob.plan(check_injective=check_injective)
+    gp = gb.plan_arrays()
+    assert gb.status() == (0, 0) and op["status"] == 0
+    for k in ("n_items", "tok_off", "hit_off", "blk_off", "item_req", "item_blk"):
+        assert np.array_equal(np.asarray(gp[k]), np.asarray(op[k])), k
+
+    R = spec.R
+    hit_out = sentinel_dev(ob.total_hit() * R)
+    complete = sentinel_dev(ob.total_tokens() * R)
+    for layer in range(spec.L):
+        gb.slice_layer(layer, hit_out)
+        st, want_hit = ob.slice_layer(layer)
+        assert st == 0
+        assert_bytes_equal(hit_out[:want_hit.size], want_hit, f"hit_layer[{layer}]")
+        assert torch.all(hit_out[want_hit.size:] == SENT)
+
+        gb.merge_scatter(layer, d.pool, complete)
+        st, want_comp = ob.merge_scatter(layer, hb.pool, want_complete=True)
+        assert st == 0
+        assert_bytes_equal(complete[:want_comp.size], want_comp, f"complete_layer[{layer}]")
+        assert_bytes_equal(d.pool, hb.pool, f"pool after merge-scatter of layer {layer}")
+
+        gb.gather(layer, d.pool)
+        assert ob.gather_objects(layer, hb.pool) == 0
+        assert_bytes_equal(d.objects, hb.objects, f"objects of layer {layer}")
+
+    # scatter back into fresh pools, layer by layer
+    d.pool.fill_(SENT)
+    hb.pool[:] = SENT
+    for layer in range(spec.L):
+        if objects_one_layer:
+            break
+        gb.scatter_back(layer, d.pool)
+        assert ob.scatter_back(layer, hb.pool) == 0
+    assert_bytes_equal(d.pool, hb.pool, "pool after scatter-back")
+    assert gb.status() == (0, 0)
+
+
+def test_tiny_workload_bit_exact():
+    run_parity(workloads.get_spec("tiny"), payload="spec")
+
+
+RANDOM_CASES = 14
+
+
+@pytest.mark.parametrize("case", range(RANDOM_CASES))
+def test_random_ragged_batches_bit_exact(case):
+    g = np.random.default_rng(9000 + case)
+    P = int(g.integers(1, 3))
+    Rp = int(g.choice([16, 48, 256, 1152, 2048]))
+    B = int(g.choice([1, 3, 16, 64]))
+    n = int(g.choice([1, 2, 7, 33]))
+    max_t = int(max(8, min(1200, 400_000 // max(1, n * Rp * P))))
+    t_hit = g.integers(0, max_t, n)
+    t_miss = g.integers(0, max(2, max_t // 4), n)
+    if case % 5 == 0:
+        t_hit[0] = 0          # a miss-only request
+    if case % 7 == 1 and n > 1:
+        t_miss[-1] = 0        # a hit-only request
+    spec = workloads.custom_spec(
+        L=int(g.integers(1, 4)), P=P, B=B, Rp=Rp, t_hit=t_hit, t_miss=t_miss,
+        table=str(g.choice(["perm", "fragmented", "identity"])),
+        source=str(g.choice(["contiguous", "permuted"])),
+        miss_order=str(g.choice(["layer", "token"])), seed=700 + case)
+    run_parity(spec)
+
+
+SCALED = {
+    # the shapes of the four larger workloads, with fewer layers and tokens
+    "llama3_8b_agentic": dict(L=3, P=2, B=16, Rp=2048, t_hit=[3000], t_miss=[77], table="perm"),
+    "qwen3_32b_long": dict(L=2, P=2, B=64, Rp=2048, t_hit=[5000], t_miss=[1700], table="perm",
+                           source="permuted"),
+    "latent_batch": dict(L=2, P=1, B=64, Rp=1152, t_hit=[1700, 900, 2500, 64, 1300],
+                         t_miss=[130, 2000, 7, 64, 1], table="perm"),
+    "many_small": dict(L=2, P=2, B=16, Rp=2048, t_hit=list(range(37, 37 + 40 * 23, 23)),
+                       t_miss=[16 + (7 * i) % 240 for i in range(40)], table="fragmented"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SCALED))
+def test_scaled_workload_shapes_bit_exact(name):
+    run_parity(workloads.custom_spec(name, **SCALED[name], seed=31))
+
+
+def test_without_injectivity_check_results_are_unchanged():
+    spec = workloads.custom_spec(L=2, P=2, B=16, Rp=256, t_hit=[300, 5], t_miss=[20, 40])
+    run_parity(spec, check_injective=False)
+
+
+def test_objects_with_zero_layer_stride():
+    spec = workloads.custom_spec(L=3, P=2, B=16, Rp=256, t_hit=[100, 50], t_miss=[3, 60])
+    run_parity(spec, objects_one_layer=True)
+
+
+# --------------------------------------------------------------------------
+# Full-size workloads, sampled layers
+# --------------------------------------------------------------------------
+
+FULL = ["llama3_8b_agentic", "qwen3_32b_long", "latent_batch", "many_small"]
+
+
+def _free_gb():
+    free, _ = torch.cuda.mem_get_info()
+    return free / 1e9
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload_sampled_layers(name):
+    from layer_wise_paged_gb300.batch import Batch
+    spec = workloads.get_spec(name)
+    one_layer = name in ("latent_batch", "many_small", "qwen3_32b_long")
+    need = workloads.footprint_bytes(spec, objects_one_layer=one_layer) / 1e9
+    if need + 8 > _free_gb():
+        pytest.skip(f"{name} needs {need:.0f} GB of device memory")
+    bufs = workloads.allocate(spec, "cuda", objects_one_layer=one_layer)
+    lay = bufs["layout"]
+    g = (spec.L, spec.P, spec.B, spec.Rp, spec.n_pool)
+    gb = Batch(g, lay.requests, bufs["hit"], bufs["miss"], bufs["objects"], bufs["tables"],
+               bufs["src_tables"])
+    gb.plan()
+    assert gb.status() == (0, 0)
+    R, layer_bytes = spec.R, spec.P * spec.n_pool * spec.B * spec.Rp
+    pool = bufs["pool"]
+    hit_out = sentinel_dev(gb.total_hit * R)
+    sampled = {0, spec.L // 2, spec.L - 1}
+    for layer in range(spec.L):
+        region = pool[layer * layer_bytes:(layer + 1) * layer_bytes]
+        before = region.cpu().numpy() if layer in sampled else None
+        gb.slice_layer(layer, hit_out)
+        gb.merge_scatter(layer, pool)
+        gb.gather(layer, pool)
+        # round trip on every layer: scatter-back into a blanked layer restores it
+        after = region.clone()
+        region.fill_(SENT)
+        gb.scatter_back(layer, pool)
+        assert torch.equal(region, after), f"{name}: scatter-back round trip, layer {layer}"
+        del after
+        if layer in sampled:
+            dev = SimpleNamespace(hit=bufs["hit"], miss=bufs["miss"], tables=bufs["tables"],
+                                  src_tables=bufs["src_tables"])
+            ob, objs, obj_offs, host_pool = one_layer_problem(spec, lay, dev, layer, before)
+            st, want_hit = ob.slice_layer(0)
+            assert st == 0
+            assert_bytes_equal(hit_out[:want_hit.size], want_hit, f"{name} hit_layer[{layer}]")
+            assert ob.merge_scatter(0, host_pool)[0] == 0
+            assert_bytes_equal(region, host_pool, f"{name} pool layer {layer}")
+            assert ob.gather_objects(0, host_pool) == 0
+            for q, o in zip(lay.requests, obj_offs):
+                nb = spec.P * (-(-(q.t_hit + q.t_miss) // spec.B)) * spec.B * spec.Rp
+                a = q.obj_off + layer * q.obj_layer_stride
+                assert_bytes_equal(bufs["objects"][a:a + nb], objs[o:o + nb],
+                                   f"{name} objects layer {layer}")
+    assert gb.status() == (0, 0)
+    del bufs, gb, pool, hit_out
+    torch.cuda.empty_cache()

@@ -249,11 +249,17 @@ def layout(spec: Spec, *, objects_one_layer: bool = False) -> Layout:
     return out
 
 
+HOST_BLOCK = 256 << 20  # CPU payloads repeat a seeded block of this many bytes
+
+
 def fill_payload(buf, kind: str, seed: int) -> None:
     """Fill a torch uint8 buffer (CPU or CUDA) with seeded KV payload, in place.
 
     "normal" = bf16 N(0, 1), "uniform2" = bf16 uniform in [-2, 2], "bytes" = uniform
-    random bytes (every bit pattern, NaNs, -0.0 and subnormals included).
+    random bytes (every bit pattern, NaNs, -0.0 and subnormals included).  On the GPU
+    every byte is drawn; on the CPU a buffer longer than HOST_BLOCK repeats its first
+    HOST_BLOCK bytes (the reshuffle copies bytes, so only the value distribution
+    matters, and drawing tens of GB on the host would take minutes).
     """
     import torch
     n = buf.numel()
@@ -261,10 +267,12 @@ def fill_payload(buf, kind: str, seed: int) -> None:
         return
     g = torch.Generator(device=buf.device)
     g.manual_seed(seed)
-    chunk = 1 << 30  # bytes per fill call, bounds temporaries on huge buffers
+    chunk = 1 << 30 if buf.device.type == "cuda" else HOST_BLOCK
     for s in range(0, n, chunk):
         part = buf[s:min(n, s + chunk)]
-        if kind == "bytes" or part.numel() % 2:
+        if buf.device.type != "cuda" and s > 0:
+            part.copy_(buf[:part.numel()])
+        elif kind == "bytes" or part.numel() % 2:
             part.copy_(torch.randint(0, 256, (part.numel(),), generator=g, device=buf.device,
                                      dtype=torch.int32).to(torch.uint8))
         elif kind == "normal":
