@@ -39,6 +39,7 @@ METRIC = "KV reshuffle HBM GB/s (read+write) and % of GB300 peak; µs per layer"
 UNIT = "GB/s"
 DEFAULT_WORKLOAD = "llama3_8b_agentic"
 FALLBACK_HBM_GBS = 6800.0
+HIT_RING = 8
 OPS = ("slice", "merge_scatter", "gather", "scatter_back")
 KERNEL_NAMES = {"slice": "kvl_slice_kernel", "merge_scatter": "kvl_merge_scatter_kernel",
                 "gather": "kvl_gather_kernel", "scatter_back": "kvl_scatter_back_kernel"}
@@ -331,35 +332,44 @@ def run_gpu(args):
     kvl.lib()
 
     spec = bench_spec(args)
-    bufs = workloads.allocate(spec, dev)
+    # The largest workloads keep one layer of objects (object layer stride 0, each
+    # layer's gather lands in the same > L2-sized region) to fit in HBM.
+    one_layer = workloads.footprint_bytes(spec) > 160e9
+    bufs = workloads.allocate(spec, dev, objects_one_layer=one_layer)
     lay = bufs["layout"]
     g = (spec.L, spec.P, spec.B, spec.Rp, spec.n_pool)
     batch = Batch(g, lay.requests, bufs["hit"], bufs["miss"], bufs["objects"], bufs["tables"],
                   bufs["src_tables"])
     pool = bufs["pool"]
-    hit_out = torch.empty(max(16, spec.L * batch.total_hit * spec.R), dtype=torch.uint8, device=dev)
+    # hit_layer[l] goes to a ring of HIT_RING per-layer buffers: each is rewritten only
+    # after several other layers' traffic has pushed its lines out of L2
+    ring = min(spec.L, HIT_RING)
     layer_hit = batch.total_hit * spec.R
-    hit_views = [hit_out[l * layer_hit:] for l in range(spec.L)]
+    hit_out = torch.empty(max(16, ring * layer_hit), dtype=torch.uint8, device=dev)
+    hit_views = [hit_out[(l % ring) * layer_hit:] for l in range(spec.L)]
     stream = torch.cuda.current_stream(dev)
-    ev = {op: [] for op in OPS}
 
-    def step(record=False):
-        batch.plan(stream=stream)
+    def make_event():
+        try:  # a record node when captured in a CUDA graph
+            return torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            return None
+
+    def step(events=None, s=None):
+        s = s or stream
+        batch.plan(stream=s)
         phases = (
-            ("slice", lambda l: batch.slice_layer(l, hit_views[l], stream)),
-            ("merge_scatter", lambda l: batch.merge_scatter(l, pool, None, stream)),
-            ("gather", lambda l: batch.gather(l, pool, stream)),
-            ("scatter_back", lambda l: batch.scatter_back(l, pool, stream)),
+            ("slice", lambda l: batch.slice_layer(l, hit_views[l], s)),
+            ("merge_scatter", lambda l: batch.merge_scatter(l, pool, None, s)),
+            ("gather", lambda l: batch.gather(l, pool, s)),
+            ("scatter_back", lambda l: batch.scatter_back(l, pool, s)),
         )
         for op, fn in phases:
             for l in range(spec.L):
-                if record:
-                    a = torch.cuda.Event(enable_timing=True)
-                    b = torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
+                if events is not None:
+                    events[op][l][0].record(s)
                     fn(l)
-                    b.record(stream)
-                    ev[op].append((a, b))
+                    events[op][l][1].record(s)
                 else:
                     fn(l)
 
@@ -371,6 +381,37 @@ def run_gpu(args):
     if code != 0:
         raise SystemExit(f"bench.py: plan status {code} detail {detail}")
 
+    # One step captured as a CUDA graph (the launches of the C-ABI calls, with a
+    # timing event recorded on the launch stream around each kernel), replayed once
+    # per timed step.  --eager launches through the C ABI from Python every step.
+    ev = None
+    graph = None
+    if not args.eager and make_event() is not None:
+        ev = {op: [(make_event(), make_event()) for _ in range(spec.L)] for op in OPS}
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            step(ev, cap)  # untimed, outside capture: the library's per-device caches
+        cap.synchronize()
+        with torch.cuda.graph(graph, stream=cap):
+            step(ev, torch.cuda.current_stream(dev))
+        stream.wait_stream(cap)
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+    eager_ev = {op: [] for op in OPS}
+
+    def timed_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            evs = {op: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                        for _ in range(spec.L)] for op in OPS}
+            step(evs)
+            for op in OPS:
+                eager_ev[op].extend(evs[op])
+
     clocks_path = ROOT / "gpurun_out" / "clocks.csv" if (ROOT / "gpurun_out").is_dir() else None
     barrier(dist, dev)
     torch.cuda.synchronize(dev)
@@ -380,7 +421,7 @@ def run_gpu(args):
         time.sleep(0.3)
         t0.record(stream)
         for _ in range(args.steps):
-            step(record=True)
+            timed_step()
         t1.record(stream)
         torch.cuda.synchronize(dev)
     barrier(dist, dev)
@@ -389,12 +430,15 @@ def run_gpu(args):
     code, detail = batch.status(stream)
     if code != 0:
         raise SystemExit(f"bench.py: status {code} detail {detail} after the timed steps")
+    # per-kernel durations: the graph's events hold the last timed step's launches;
+    # eager mode keeps every timed launch
+    ev_used = ev if graph is not None else eager_ev
 
     sb = step_bytes(spec)
     value = world * sb * args.steps / elapsed / 1e9
     per_op = {}
     for op in OPS:
-        ts = [a.elapsed_time(b) / 1e3 for a, b in ev[op]]
+        ts = [a.elapsed_time(b) / 1e3 for a, b in ev_used[op]]
         avg = sum(ts) / len(ts)
         per_op[op] = {"us_per_launch": round(avg * 1e6, 2),
                       "gbs": round(op_bytes(spec)[op] / avg / 1e9, 1),
@@ -427,7 +471,10 @@ def run_gpu(args):
             bufs["hit"].copy_(h_hit, non_blocking=True)
             bufs["miss"].copy_(h_miss, non_blocking=True)
             bufs["tables"].copy_(h_tab, non_blocking=True)
-            step()
+            if graph is not None:
+                graph.replay()
+            else:
+                step()
             h_obj.copy_(bufs["objects"], non_blocking=True)
 
         for _ in range(2):
@@ -458,7 +505,13 @@ def run_gpu(args):
 
     if rank == 0:
         cfg = describe(spec)
-        cfg.update(us_per_layer=round(elapsed / args.steps / spec.L * 1e6, 2),
+        cfg.update(objects="one layer (layer stride 0)" if one_layer else "all layers",
+                   hit_layer_buffers=ring,
+                   us_per_layer=round(elapsed / args.steps / spec.L * 1e6, 2),
+                   launch="CUDA graph of one step, replayed per step" if graph is not None
+                   else "eager C-ABI calls from Python",
+                   kernel_timing="events around each launch of the last timed step"
+                   if graph is not None else "events around every timed launch",
                    step_bytes=sb, kernels=kernels, launches_per_step=launches_per_step,
                    parallelism=f"{world} independent replica(s)", gpu=torch.cuda.get_device_name(dev))
         line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -487,6 +540,8 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--eager", action="store_true",
+                   help="launch every call from Python instead of replaying a CUDA graph")
     p.add_argument("--no-cpu-baseline", action="store_true")
     a = p.parse_args(argv)
     if a.warmup < 3:

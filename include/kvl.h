@@ -52,6 +52,7 @@
  * B*Rp), so a partial block's object carries whatever those slots hold.
  *
  * Alignment: Rp, every stride and every buffer address must be multiples of 16 bytes.
+ * Size: Rp, and R for kvl_slice_layer, at most 32 KiB (one shared-memory stage).
  * Aliasing: sources, pool, objects and outputs must not overlap (undefined otherwise);
  * with an injective block table every destination byte has exactly one writer.
  *
@@ -84,6 +85,7 @@ typedef int32_t kvl_status;
 #define KVL_ERANGE 3 /* block id outside the pool / source, or plan capacity exceeded */
 #define KVL_EDUP 4   /* a pool block id used twice (only with check_injective) */
 #define KVL_ECUDA 5  /* a CUDA launch or copy failed */
+#define KVL_ETIMEOUT 6 /* a copy kernel's bounded wait on its own copies ran out (detail = CTA) */
 
 #define KVL_GATHER 0      /* kvl_gather_layer_objects: pool -> objects */
 #define KVL_SCATTER_BACK 1 /* kvl_gather_layer_objects: objects -> pool */

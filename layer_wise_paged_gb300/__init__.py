@@ -18,10 +18,10 @@ import numpy as np
 
 from .build import LIB, build
 
-KVL_OK, KVL_EINVAL, KVL_EALIGN, KVL_ERANGE, KVL_EDUP, KVL_ECUDA = range(6)
+KVL_OK, KVL_EINVAL, KVL_EALIGN, KVL_ERANGE, KVL_EDUP, KVL_ECUDA, KVL_ETIMEOUT = range(7)
 KVL_GATHER, KVL_SCATTER_BACK = 0, 1
 STATUS_NAMES = {0: "KVL_OK", 1: "KVL_EINVAL", 2: "KVL_EALIGN", 3: "KVL_ERANGE", 4: "KVL_EDUP",
-                5: "KVL_ECUDA"}
+                5: "KVL_ECUDA", 6: "KVL_ETIMEOUT"}
 
 
 class KvlError(RuntimeError):

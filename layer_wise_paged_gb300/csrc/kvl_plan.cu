@@ -266,6 +266,7 @@ extern "C" const char *kvl_status_string(kvl_status s)
     case KVL_ERANGE: return "block id out of range or plan capacity exceeded";
     case KVL_EDUP: return "pool block id used twice";
     case KVL_ECUDA: return "CUDA error";
+    case KVL_ETIMEOUT: return "a copy kernel's bounded wait on its own copies ran out";
     default: return "unknown status";
     }
 }

@@ -78,7 +78,7 @@ def test_plan_layout_is_consistent(lib):
 
 
 def test_status_strings_and_launch_counts(lib):
-    for c in range(6):
+    for c in range(7):
         assert kvl.kvl_status_string(c)
     assert kvl.kvl_launches_per_call(0) == 2
     assert [kvl.kvl_launches_per_call(w) for w in (1, 2, 3)] == [1, 1, 1]
