@@ -150,6 +150,33 @@ kvl_status kvl_batch_plan(const kvl_geom *geom, int32_t n_req, const kvl_request
                           const int32_t *d_block_tables, int32_t check_injective,
                           void *d_plan, size_t plan_bytes, void *stream);
 
+/* kvl_batch_plan_static_scratch -- kvl_batch_plan for callers that cannot allocate
+ * device memory.  The pages have no counterpart to this call.
+ * Some callers cannot call cudaMalloc: for instance an inference engine whose own
+ * allocator owns all of the HBM (its KV pool took it up front), where an extra
+ * scratch allocation would fail or break the engine's accounting.  This call needs
+ * no scratch from the caller: the injectivity bitmap lives in a fixed device array
+ * inside libkvl.so (KVL_STATIC_SCRATCH_POOL_BLOCKS / 8 bytes = 512 KiB, held by
+ * every GPU that loads the library until the process exits).  The caller still
+ * passes the requests, the block tables and the plan, and the plan needs only
+ * kvl_plan_layout(...)[6] bytes (everything before the bitmap section); the plan it
+ * writes is the same as kvl_batch_plan's and the copy calls accept it.
+ * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ * The first call on a device looks up the array's device address (once per device,
+ * with that device current) and caches it; make that first call before any stream
+ * capture.
+ * Limits and sharing: pool_blocks above KVL_STATIC_SCRATCH_POOL_BLOCKS returns
+ * KVL_EINVAL and launches nothing.  Every call on a device shares the one array,
+ * which keeps the last call's contents; each call clears the bits it uses before
+ * using them, but calls that overlap on the GPU (other streams, other host threads)
+ * race on the array and may report duplicates wrongly.  Other arguments, checks and
+ * status codes are those of kvl_batch_plan. */
+#define KVL_STATIC_SCRATCH_POOL_BLOCKS (1 << 22)
+kvl_status kvl_batch_plan_static_scratch(const kvl_geom *geom, int32_t n_req,
+                                         const kvl_request *d_reqs, const int32_t *d_block_tables,
+                                         int32_t check_injective, void *d_plan, size_t plan_bytes,
+                                         void *stream);
+
 /* kvl_slice_layer -- hit_layer[l] = hit_full_block[:, l] for every request
  * (DualPath KV Loading, "Dual-Path Loading": objects table and the slice_layer step
  * of pe_read_path / de_read_path).  Writes sum(T_hit) rows of R bytes to d_hit_out

@@ -62,13 +62,14 @@ def lib():
         L.kvl_plan_bytes.argtypes, L.kvl_plan_bytes.restype = [i32, i64], sz
         L.kvl_plan_layout.argtypes, L.kvl_plan_layout.restype = [i32, i64, ctypes.POINTER(sz)], None
         L.kvl_batch_plan.argtypes = [gp, i32, vp, vp, i32, vp, sz, vp]
+        L.kvl_batch_plan_static_scratch.argtypes = [gp, i32, vp, vp, i32, vp, sz, vp]
         L.kvl_slice_layer.argtypes = [gp, vp, vp, i32, vp, vp]
         L.kvl_merge_scatter_paged.argtypes = [gp, vp, vp, vp, i32, vp, vp, vp]
         L.kvl_gather_layer_objects.argtypes = [gp, vp, vp, vp, i32, vp, i32, vp]
         L.kvl_read_status.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i64), vp]
         L.kvl_status_string.argtypes, L.kvl_status_string.restype = [i32], ctypes.c_char_p
         L.kvl_launches_per_call.argtypes, L.kvl_launches_per_call.restype = [i32], i32
-        for f in (L.kvl_batch_plan, L.kvl_slice_layer, L.kvl_merge_scatter_paged,
+        for f in (L.kvl_batch_plan, L.kvl_batch_plan_static_scratch, L.kvl_slice_layer, L.kvl_merge_scatter_paged,
                   L.kvl_gather_layer_objects, L.kvl_read_status):
             f.restype = i32
         _lib = L
@@ -104,6 +105,18 @@ def kvl_batch_plan(g, n_req, d_reqs, d_block_tables, check_injective, d_plan, pl
     return int(lib().kvl_batch_plan(_g(g), int(n_req), _p(d_reqs), _p(d_block_tables),
                                     int(bool(check_injective)), _p(d_plan), int(plan_bytes),
                                     _p(stream)))
+
+
+def kvl_batch_plan_static_scratch(g, n_req, d_reqs, d_block_tables, check_injective, d_plan,
+                                  plan_bytes, stream=None) -> int:
+    """kvl_batch_plan for callers that cannot allocate device memory: its scratch is a
+    fixed array inside the library (pool_blocks <= KVL_STATIC_SCRATCH_POOL_BLOCKS)."""
+    return int(lib().kvl_batch_plan_static_scratch(_g(g), int(n_req), _p(d_reqs),
+                                                   _p(d_block_tables), int(bool(check_injective)),
+                                                   _p(d_plan), int(plan_bytes), _p(stream)))
+
+
+KVL_STATIC_SCRATCH_POOL_BLOCKS = 1 << 22
 
 
 def kvl_slice_layer(g, d_plan, d_reqs, layer, d_hit_out, stream=None) -> int:
@@ -177,6 +190,7 @@ def pack_requests(requests, *, hit_base=0, miss_base=0, obj_base=0, src_table_ba
 
 
 __all__ = ["build", "lib", "geom", "kvl_geom", "REQUEST_DTYPE", "pack_requests", "check",
-           "KvlError", "kvl_plan_bytes", "kvl_plan_layout", "kvl_batch_plan", "kvl_slice_layer",
+           "KvlError", "kvl_plan_bytes", "kvl_plan_layout", "kvl_batch_plan", "kvl_batch_plan_static_scratch",
+           "kvl_slice_layer",
            "kvl_merge_scatter_paged", "kvl_gather_layer_objects", "kvl_read_status",
            "kvl_status_string", "kvl_launches_per_call"]

@@ -12,6 +12,7 @@
 #include <climits>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "kvl_internal.cuh"
 
@@ -278,4 +279,81 @@ extern "C" int32_t kvl_launches_per_call(int32_t which)
     case 1: case 2: case 3: return 1;
     default: return 0;
     }
+}
+
+// ---------------------------------------------------------------------------
+// kvl_batch_plan_static_scratch: the plan builder for callers that cannot
+// allocate device memory.  Its only scratch, the injectivity bitmap, lives in the
+// file-scope array below instead of the caller's plan buffer.  The array is a
+// fixed KVL_STATIC_SCRATCH_POOL_BLOCKS / 8 bytes (512 KiB) that every GPU which
+// loads this library holds until the process exits.
+// ---------------------------------------------------------------------------
+
+namespace kvl {
+namespace {
+
+static __device__ __align__(256) uint32_t g_plan_bitmap[KVL_STATIC_SCRATCH_POOL_BLOCKS / 32];
+
+// Host code must not pass g_plan_bitmap itself to a kernel: on the host that name
+// is a stand-in, not a device address.  The device address is looked up once per
+// device, with that device current, and cached here.
+uint32_t *g_plan_bitmap_dev[kMaxDevices] = {nullptr};
+std::mutex g_plan_bitmap_mutex;
+
+kvl_status static_bitmap_address(uint32_t **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVL_ECUDA;
+    std::lock_guard<std::mutex> lock(g_plan_bitmap_mutex);
+    if (g_plan_bitmap_dev[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_plan_bitmap) != cudaSuccess || p == nullptr) return KVL_ECUDA;
+        g_plan_bitmap_dev[dev] = static_cast<uint32_t *>(p);
+    }
+    *out = g_plan_bitmap_dev[dev];
+    return KVL_OK;
+}
+
+}  // namespace
+}  // namespace kvl
+
+extern "C" kvl_status kvl_batch_plan_static_scratch(const kvl_geom *geom, int32_t n_req,
+                                                    const kvl_request *d_reqs,
+                                                    const int32_t *d_block_tables,
+                                                    int32_t check_injective, void *d_plan,
+                                                    size_t plan_bytes, void *stream)
+{
+    const kvl_status g = check_geom(geom);
+    if (g) return g;
+    if (geom->pool_blocks > KVL_STATIC_SCRATCH_POOL_BLOCKS) return KVL_EINVAL;
+    if (n_req < 0 || !d_plan) return KVL_EINVAL;
+    if (n_req > 0 && (!d_reqs || !d_block_tables)) return KVL_EINVAL;
+    if (!aligned16(d_plan) || (d_reqs && !aligned16(d_reqs)) ||
+        (reinterpret_cast<uintptr_t>(d_block_tables) & 3u))
+        return KVL_EALIGN;
+    // everything of the plan but its bitmap section
+    if (plan_bytes < plan_layout(n_req, geom->pool_blocks).off[6]) return KVL_EINVAL;
+
+    uint32_t *bitmap = nullptr;
+    const kvl_status sa = static_bitmap_address(&bitmap);
+    if (sa) return sa;
+
+    PlanArgs a;
+    a.v = plan_view(d_plan, n_req, geom->pool_blocks);
+    a.v.bitmap = bitmap;  // the scan kernel clears the words it uses on every call
+    a.reqs = d_reqs;
+    a.tables = d_block_tables;
+    a.n_req = n_req;
+    a.B = geom->block_tokens;
+    a.N = geom->pool_blocks;
+    a.check_injective = check_injective ? 1 : 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    plan_scan_kernel<<<1, kScanThreads, 0, s>>>(a);
+    if (launch_status()) return KVL_ECUDA;
+    const int sms = sm_count();
+    if (sms <= 0) return KVL_ECUDA;
+    int64_t want = (geom->pool_blocks + kFillThreads - 1) / kFillThreads;
+    int grid = int(want < int64_t(sms) * 4 ? (want < 1 ? 1 : want) : int64_t(sms) * 4);
+    plan_fill_kernel<<<grid, kFillThreads, 0, s>>>(a);
+    return launch_status();
 }
