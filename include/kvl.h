@@ -117,16 +117,18 @@ typedef struct kvl_request {
     int32_t t_miss;
 } kvl_request;
 
-/* Bytes of device memory a plan for n_req requests over a pool of pool_blocks needs.
- * The plan holds at most pool_blocks work items: injective tables never need more. */
-size_t kvl_plan_bytes(int32_t n_req, int64_t pool_blocks);
+/* Bytes of device memory a plan for n_req requests in this geometry needs (0 for a
+ * bad geometry).  The plan holds at most pool_blocks work items (injective tables
+ * never need more), a 128-byte record per item and a claim counter per (layer, op). */
+size_t kvl_plan_bytes(const kvl_geom *geom, int32_t n_req);
 
 /* Plan layout, for callers that read the plan's arrays (byte offsets into the plan):
  * off[0] header, off[1] tok_off (int64[n_req+1]), off[2] hit_off (int64[n_req+1]),
  * off[3] blk_off (int64[n_req+1]), off[4] item_req (int32[pool_blocks]),
- * off[5] item_blk (int32[pool_blocks]), off[6] injectivity bitmap, off[7] total bytes.
- * The header's first int32 is the status and its int64 at byte 16 the item count. */
-void kvl_plan_layout(int32_t n_req, int64_t pool_blocks, size_t off[8]);
+ * off[5] item_blk (int32[pool_blocks]), off[6] item records, off[7] claim counters,
+ * off[8] injectivity bitmap, off[9] total bytes.  The header's first int32 is the
+ * status and its int64 at byte 16 the item count. */
+void kvl_plan_layout(const kvl_geom *geom, int32_t n_req, size_t off[10]);
 
 /* kvl_batch_plan -- the batch's work list, built on the device.
  * Computes exclusive prefix sums over requests of T_all (tok_off), T_hit (hit_off)
@@ -141,8 +143,13 @@ void kvl_plan_layout(int32_t n_req, int64_t pool_blocks, size_t off[8]);
  *   geom            host pointer
  *   d_reqs          device array of n_req requests (caller-owned, read only)
  *   d_block_tables  device int32 tables, packed in request order (read only)
- *   d_plan          device buffer of plan_bytes >= kvl_plan_bytes(n_req, N) bytes,
- *                   16-byte aligned, caller-owned; overwritten
+ *   d_plan          device buffer of plan_bytes >= kvl_plan_bytes(geom, n_req) bytes,
+ *                   16-byte aligned, caller-owned; overwritten.  The plan resolves
+ *                   every item's addresses and block ids when it is built: later
+ *                   edits to the requests or tables take effect only through a new
+ *                   plan.  The copy calls update the plan's claim counters, so two
+ *                   calls on one plan for the same layer and op must not overlap on
+ *                   the GPU (calls for different layers or ops may).
  * Device-side status: EINVAL (detail = first bad request), EALIGN (detail = first bad
  * request), ERANGE (detail = smallest bad work item, or the item count when it
  * exceeds N), EDUP (detail = smallest repeated block id).  The largest code wins. */
@@ -159,7 +166,7 @@ kvl_status kvl_batch_plan(const kvl_geom *geom, int32_t n_req, const kvl_request
  * inside libkvl.so (KVL_STATIC_SCRATCH_POOL_BLOCKS / 8 bytes = 512 KiB, held by
  * every GPU that loads the library until the process exits).  The caller still
  * passes the requests, the block tables and the plan, and the plan needs only
- * kvl_plan_layout(...)[6] bytes (everything before the bitmap section); the plan it
+ * kvl_plan_layout(...)[8] bytes (everything before the bitmap section); the plan it
  * writes is the same as kvl_batch_plan's and the copy calls accept it.
  * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
  * The first call on a device looks up the array's device address (once per device,

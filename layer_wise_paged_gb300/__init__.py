@@ -59,8 +59,8 @@ def lib():
         L = ctypes.CDLL(str(LIB))
         vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
         gp = ctypes.POINTER(kvl_geom)
-        L.kvl_plan_bytes.argtypes, L.kvl_plan_bytes.restype = [i32, i64], sz
-        L.kvl_plan_layout.argtypes, L.kvl_plan_layout.restype = [i32, i64, ctypes.POINTER(sz)], None
+        L.kvl_plan_bytes.argtypes, L.kvl_plan_bytes.restype = [gp, i32], sz
+        L.kvl_plan_layout.argtypes, L.kvl_plan_layout.restype = [gp, i32, ctypes.POINTER(sz)], None
         L.kvl_batch_plan.argtypes = [gp, i32, vp, vp, i32, vp, sz, vp]
         L.kvl_batch_plan_static_scratch.argtypes = [gp, i32, vp, vp, i32, vp, sz, vp]
         L.kvl_slice_layer.argtypes = [gp, vp, vp, i32, vp, vp]
@@ -90,13 +90,13 @@ def _p(x):
     return None if x is None or x == 0 else ctypes.c_void_p(int(x))
 
 
-def kvl_plan_bytes(n_req: int, pool_blocks: int) -> int:
-    return int(lib().kvl_plan_bytes(int(n_req), int(pool_blocks)))
+def kvl_plan_bytes(g, n_req: int) -> int:
+    return int(lib().kvl_plan_bytes(_g(g), int(n_req)))
 
 
-def kvl_plan_layout(n_req: int, pool_blocks: int) -> list:
-    off = (ctypes.c_size_t * 8)()
-    lib().kvl_plan_layout(int(n_req), int(pool_blocks), off)
+def kvl_plan_layout(g, n_req: int) -> list:
+    off = (ctypes.c_size_t * 10)()
+    lib().kvl_plan_layout(_g(g), int(n_req), off)
     return [int(x) for x in off]
 
 

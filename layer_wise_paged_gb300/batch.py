@@ -49,9 +49,9 @@ class Batch:
         if raw.size == 0:
             raw = np.zeros(96, np.uint8)
         self.d_reqs = torch.from_numpy(raw.copy()).to(self.device)
-        self.plan_bytes = kvl_plan_bytes(self.n_req, self.N)
+        self.plan_bytes = kvl_plan_bytes(self.g, self.n_req)
         self.d_plan = torch.zeros(self.plan_bytes, dtype=torch.uint8, device=self.device)
-        self.layout = kvl_plan_layout(self.n_req, self.N)
+        self.layout = kvl_plan_layout(self.g, self.n_req)
         self.total_hit = int(sum(q.t_hit for q in self.requests))
         self.total_tokens = int(sum(q.t_hit + q.t_miss for q in self.requests))
         self.n_items = int(sum(-(-(q.t_hit + q.t_miss) // self.B) for q in self.requests))

@@ -1,29 +1,34 @@
 // kvl_copy.cu -- the per-layer copy kernels of libkvl.so: slice, merge-scatter into
 // the paged pool, and gather / scatter-back of per-layer K/V objects.
 //
-// Every op walks a flat "row space": the rows of all work items of the plan, item by
-// item (then plane by plane, then slot by slot).  A row is one token's Rp-byte plane
-// (merge-scatter, gather, scatter-back) or one token's R-byte layer row (slice).
-// Each CTA of a persistent grid takes one contiguous, equal share of the row space
-// (balanced to within one row whatever the request mix) and cuts it into segments:
-// runs of rows of one (item, plane) whose destination is one contiguous range, at
-// most one shared-memory stage long.
+// Work unit: one work item of the plan, i.e. one logical block j of one request
+// (Tutti 阅读笔记, 伪代码 1: retrieve_layer walks a layer's block ids; here every
+// (request, block) of the batch is one item of a single launch per layer).  Its rows
+// are the block's token slots of each plane (merge-scatter, gather, scatter-back) or
+// the block's token rows of the layer (slice).
 //
-// A CTA is one warp driving the Tensor Memory Accelerator's bulk copies:
-//   * metadata: each lane decodes one work item (request, block, pool block id,
-//     source block id, row bases) with plain loads, in parallel, and the warp reads
-//     each item's fields from its owner lane with shuffles;
-//   * loads: `cp.async.bulk` global -> shared, one per source row (rows of one token
-//     plane are not adjacent in the full-block source), or one per segment when the
-//     source run is contiguous (gather / scatter-back), completing on a stage's
-//     mbarrier;
-//   * stores: one `cp.async.bulk` shared -> global per segment (the destination run
-//     is contiguous), in bulk groups; a stage is refilled only after its store has
-//     read it (`cp.async.bulk.wait_group.read`).
-// Loads run up to kStages - 1 segments ahead of stores, so each SM keeps well over
-// 100 KiB in flight with no registers holding data.  Every mbarrier wait is bounded
-// by the global timer: past the limit the kernel records KVL_ETIMEOUT, waits
-// (bounded again) for its copies in flight and returns.
+// A CTA is one warp driving the Tensor Memory Accelerator's bulk copies, on every
+// SM of a persistent grid:
+//   * scheduling: CTA b takes item b, then claims further items one at a time from a
+//     per-(layer, op) counter in the plan (atomicAdd, issued one item ahead), so
+//     faster SMs take more items and all finish together; the last CTA to finish
+//     resets the counter for the next launch;
+//   * metadata: the plan resolved every item into a 128-byte record (bases and
+//     strides at layer 0, pool block id, hit / valid slot counts); the warp loads the
+//     next item's record (one word per lane) while the current item's copies run,
+//     and reads fields from their lanes with shuffles;
+//   * loads: `cp.async.bulk` global -> shared, one per source row (a token's plane is
+//     not adjacent to the next token's in the full-block source), or one per segment
+//     when the source run is contiguous (gather / scatter-back), completing on the
+//     stage's mbarrier;
+//   * stores: one `cp.async.bulk` shared -> global per segment (a segment is a run of
+//     slots of one item and plane, at most one stage long, whose destination is
+//     contiguous), in bulk groups; a stage is refilled only after its store has read
+//     it (`cp.async.bulk.wait_group.read`).
+// Loads run up to kStages - 1 segments ahead of stores across item boundaries, so
+// each SM keeps well over 100 KiB in flight with no registers holding data.  Every
+// mbarrier wait is bounded by the global timer: past the limit the kernel records
+// KVL_ETIMEOUT, waits (bounded again) for its copies in flight and returns.
 #include <cstdint>
 
 #include "kvl_internal.cuh"
@@ -59,7 +64,7 @@ struct CopyArgs {
     const int32_t *tables;
     uint8_t *pool;
     uint8_t *out;  // hit_out (slice), complete_out (merge, may be null)
-    int32_t P, B, Rp, layer;
+    int32_t P, B, Rp, layer, L;
     int64_t N;
 };
 
@@ -201,105 +206,80 @@ __device__ __forceinline__ bool plan_usable(const CopyArgs &a)
 {
     PlanHeader *h = static_cast<PlanHeader *>(a.plan);
     if (h->magic != kPlanMagic || h->pool_blocks != a.N || h->block_tokens != a.B ||
-        h->reqs != a.reqs || (OP != OP_SLICE && h->tables != a.tables)) {
+        h->n_layers != a.L || h->reqs != a.reqs || (OP != OP_SLICE && h->tables != a.tables)) {
         if (blockIdx.x == 0 && threadIdx.x == 0) record_error(h, KVL_EINVAL, 0);
         return false;
     }
     return h->status == KVL_OK;
 }
 
-// Decode work item `item` of layer a.layer.  Returns false (after recording the
-// error) when a block id is out of range or a needed pointer is missing.
-template <int OP>
-__device__ bool item_meta(const CopyArgs &a, const PlanView &v, int64_t item, ItemMeta &m)
-{
-    const int r = v.item_req[item];
-    const int64_t j = v.item_blk[item];
-    const kvl_request &q = a.reqs[r];
-    const int64_t B = a.B, Rp = a.Rp, l = a.layer, t0 = j * B;
-    const int64_t t_hit = q.t_hit, t_all = t_hit + q.t_miss;
-    m.src_a = m.src_b = nullptr;
-    m.dst = m.dst2 = nullptr;
-    m.a_stride = m.b_stride = m.src_pstride = m.dst_pstride = 0;
-    const int64_t n_a = t_hit - t0 < 0 ? 0 : (t_hit - t0 > B ? B : t_hit - t0);
-    const int64_t n_v = t_all - t0 < 0 ? 0 : (t_all - t0 > B ? B : t_all - t0);
-    m.n_a = int32_t(n_a);
-    m.n_valid = int32_t(n_v);
+// Field of the item record held one word per lane.
+__device__ __forceinline__ uint32_t rec_word(uint32_t rec, int w) { return __shfl_sync(0xffffffffu, rec, w); }
 
-    if (OP == OP_SLICE || OP == OP_MERGE) {
-        if (n_a > 0) {
-            const int64_t sb = q.hit_src_table ? int64_t(q.hit_src_table[j]) : j;
-            if (sb < 0 || sb >= q.hit_src_blocks) {
-                record_error(v.hdr, KVL_ERANGE, (unsigned long long)item);
-                return false;
-            }
-            m.src_a = static_cast<const uint8_t *>(q.hit_src) + sb * q.hit_block_stride +
-                      l * q.hit_layer_stride;
-            m.a_stride = q.hit_token_stride;
-        }
-        if (OP == OP_SLICE) {
-            m.n_valid = m.n_a;
-            m.dst = a.out + (v.hit_off[r] + t0) * (int64_t(a.P) * Rp);
-            return true;
-        }
-        if (n_v > n_a) {
-            // row s >= n_a is miss token t0 + s - t_hit
-            m.src_b = static_cast<const uint8_t *>(q.miss_src) + (t0 - t_hit) * q.miss_token_stride +
-                      l * q.miss_layer_stride;
-            m.b_stride = q.miss_token_stride;
-        }
-        m.src_pstride = Rp;
-        if (a.out) m.dst2 = a.out + (v.tok_off[r] + t0) * (int64_t(a.P) * Rp);
-    }
-    const int64_t b = a.tables[v.blk_off[r] + j];
-    if (b < 0 || b >= a.N) {
-        record_error(v.hdr, KVL_ERANGE, (unsigned long long)item);
-        return false;
-    }
-    uint8_t *pool_blk = a.pool + ((l * a.P) * a.N + b) * B * Rp;
-    const int64_t pool_pstride = a.N * B * Rp;
-    if (OP == OP_MERGE) {
-        m.dst = pool_blk;
-        m.dst_pstride = pool_pstride;
-        return true;
-    }
-    if (q.objects == nullptr) {
-        record_error(v.hdr, KVL_EINVAL, (unsigned long long)r);
-        return false;
-    }
-    const int64_t nblk = v.blk_off[r + 1] - v.blk_off[r];
-    uint8_t *obj = static_cast<uint8_t *>(q.objects) + l * q.obj_layer_stride + j * B * Rp;
-    const int64_t obj_pstride = nblk * B * Rp;
-    m.n_a = m.n_valid = int32_t(B);  // objects carry whole blocks
-    if (OP == OP_GATHER) {
-        m.src_a = pool_blk;
-        m.src_pstride = pool_pstride;
-        m.dst = obj;
-        m.dst_pstride = obj_pstride;
-    } else {
-        m.src_a = obj;
-        m.src_pstride = obj_pstride;
-        m.dst = pool_blk;
-        m.dst_pstride = pool_pstride;
-    }
-    m.a_stride = Rp;
-    return true;
+__device__ __forceinline__ uint64_t rec_u64(uint32_t rec, int w)
+{
+    return uint64_t(rec_word(rec, w)) | (uint64_t(rec_word(rec, w + 1)) << 32);
 }
 
-__device__ __forceinline__ ItemMeta shfl_meta(const ItemMeta &m, int src)
+// The bases and strides the item's rows are copied through, for this op and layer,
+// from the item's record.  False (after recording the error) when this op cannot
+// copy the item.
+template <int OP>
+__device__ __forceinline__ bool item_meta(const CopyArgs &a, PlanHeader *h, uint32_t rec, ItemMeta &m)
 {
-    ItemMeta o;
-    o.src_a = shfl_ptr(m.src_a, src);
-    o.src_b = shfl_ptr(m.src_b, src);
-    o.dst = shfl_ptr(m.dst, src);
-    o.dst2 = shfl_ptr(m.dst2, src);
-    o.a_stride = __shfl_sync(0xffffffffu, m.a_stride, src);
-    o.b_stride = __shfl_sync(0xffffffffu, m.b_stride, src);
-    o.src_pstride = __shfl_sync(0xffffffffu, m.src_pstride, src);
-    o.dst_pstride = __shfl_sync(0xffffffffu, m.dst_pstride, src);
-    o.n_a = __shfl_sync(0xffffffffu, m.n_a, src);
-    o.n_valid = __shfl_sync(0xffffffffu, m.n_valid, src);
-    return o;
+    const int64_t l = a.layer, B = a.B, Rp = a.Rp;
+    const int64_t b = int32_t(rec_word(rec, 22));
+    const int32_t n_hit = int32_t(rec_word(rec, 23));
+    const int32_t n_valid = int32_t(rec_word(rec, 24));
+    const int32_t req = int32_t(rec_word(rec, 25));
+    const uint64_t hit_base = rec_u64(rec, 0), miss_base = rec_u64(rec, 6), obj_base = rec_u64(rec, 12);
+    const int64_t hit_ts = int64_t(rec_u64(rec, 2)), hit_ls = int64_t(rec_u64(rec, 4));
+    const int64_t miss_ts = int64_t(rec_u64(rec, 8)), miss_ls = int64_t(rec_u64(rec, 10));
+    const int64_t obj_ps = int64_t(rec_u64(rec, 14)), obj_ls = int64_t(rec_u64(rec, 16));
+    const int64_t hit_row = int64_t(rec_u64(rec, 18)), tok_row = int64_t(rec_u64(rec, 20));
+    const int64_t R = int64_t(a.P) * Rp;
+    m.src_a = reinterpret_cast<const uint8_t *>(hit_base + uint64_t(l * hit_ls));
+    m.src_b = reinterpret_cast<const uint8_t *>(miss_base + uint64_t(l * miss_ls));
+    m.a_stride = hit_ts;
+    m.b_stride = miss_ts;
+    m.n_a = n_hit;
+    m.n_valid = n_valid;
+    m.dst2 = nullptr;
+    uint8_t *pool_blk = a.pool + ((l * a.P) * a.N + b) * B * Rp;
+    const int64_t pool_ps = a.N * B * Rp;
+    if (OP == OP_SLICE) {
+        m.n_valid = n_hit;
+        m.src_pstride = 0;
+        m.dst = a.out + hit_row * R;
+        m.dst_pstride = 0;
+        return true;
+    }
+    if (OP == OP_MERGE) {
+        m.src_pstride = Rp;
+        m.dst = pool_blk;
+        m.dst_pstride = pool_ps;
+        if (a.out) m.dst2 = a.out + tok_row * R;
+        return true;
+    }
+    if (obj_base == 0) {
+        if ((threadIdx.x & 31) == 0) record_error(h, KVL_EINVAL, (unsigned long long)req);
+        return false;
+    }
+    uint8_t *obj = reinterpret_cast<uint8_t *>(obj_base + uint64_t(l * obj_ls));
+    m.n_a = m.n_valid = int32_t(B);  // objects carry whole blocks
+    m.a_stride = Rp;
+    if (OP == OP_GATHER) {
+        m.src_a = pool_blk;
+        m.src_pstride = pool_ps;
+        m.dst = obj;
+        m.dst_pstride = obj_ps;
+    } else {
+        m.src_a = obj;
+        m.src_pstride = obj_ps;
+        m.dst = pool_blk;
+        m.dst_pstride = pool_ps;
+    }
+    return true;
 }
 
 // ---- the pipelined copy --------------------------------------------------------
@@ -324,15 +304,14 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
     allow_dependents_launch();
     if (!plan_usable<OP>(a)) return;
     PlanHeader *h = static_cast<PlanHeader *>(a.plan);
-    const PlanView v = plan_view(a.plan, h->n_req, h->pool_blocks);
+    const PlanView v = plan_view(a.plan, h->n_req, h->pool_blocks, h->n_layers);
+    const int64_t n_items = h->n_items;
+    ClaimCounter *ctr = &v.counters[int64_t(a.layer) * kOps + OP];
+    const int64_t G = gridDim.x;
+
     const int planes = OP == OP_SLICE ? 1 : a.P;
-    const int rpi = planes * a.B;                        // rows per item
     const int row_bytes = OP == OP_SLICE ? a.P * a.Rp : a.Rp;
-    const int max_rows = kStageBytes / row_bytes;        // >= 1 (host-checked)
-    const int64_t total = h->n_items * rpi;
-    const int64_t begin = total * blockIdx.x / gridDim.x;
-    const int64_t end = total * (blockIdx.x + 1) / gridDim.x;
-    if (begin >= end) return;
+    const int max_rows = kStageBytes / row_bytes;  // >= 1 (host-checked)
     const int64_t R = int64_t(a.P) * a.Rp;
 
     const uint32_t smem0 = smem_u32(smem);
@@ -367,31 +346,31 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
         ++retired;
     };
 
-    const int64_t item_first = begin / rpi;
-    const int64_t item_last = (end - 1) / rpi;
-    for (int64_t ib = item_first; ib <= item_last && !timed_out; ib += 32) {
-        // each lane decodes one item of this batch
-        ItemMeta mine{};
-        bool ok_mine = false;
-        if (ib + lane <= item_last) ok_mine = item_meta<OP>(a, v, ib + lane, mine);
-        const unsigned ok_mask = __ballot_sync(0xffffffffu, ok_mine);
-        const int nb = int(item_last - ib + 1 < 32 ? item_last - ib + 1 : 32);
-        for (int k = 0; k < nb && !timed_out; ++k) {
-            if (!((ok_mask >> k) & 1u)) continue;
-            const ItemMeta m = shfl_meta(mine, k);
-            const int64_t item = ib + k;
-            const int64_t item_row0 = item * rpi;
-            const int64_t lo = begin > item_row0 ? begin - item_row0 : 0;
-            const int64_t hi = end - item_row0 < rpi ? end - item_row0 : rpi;
-            for (int p = int(lo / a.B); p < planes && int64_t(p) * a.B < hi && !timed_out; ++p) {
-                // slots [s_lo, s_hi) of plane p inside this CTA's share, clipped to valid rows
-                int64_t s_lo = lo - int64_t(p) * a.B;
-                if (s_lo < 0) s_lo = 0;
-                int64_t s_hi = hi - int64_t(p) * a.B;
-                if (s_hi > a.B) s_hi = a.B;
-                if (s_hi > m.n_valid) s_hi = m.n_valid;
-                for (int64_t s0 = s_lo; s0 < s_hi && !timed_out; s0 += max_rows) {
-                    const int ns = int(s_hi - s0 < max_rows ? s_hi - s0 : max_rows);
+    auto load_rec = [&](int64_t item) -> uint32_t {
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(v.items + item);
+        return __ldg(w + lane);
+    };
+
+    // CTA b starts on item b; later items are claimed from the counter (its values
+    // count from the G statically placed items), one claim in flight ahead.
+    int64_t cur = blockIdx.x;
+    uint32_t rec_cur = cur < n_items ? load_rec(cur) : 0u;
+    uint32_t claim = 0;
+    if (lane == 0) claim = atomicAdd(&ctr->next, 1u);
+    for (;;) {
+        const int64_t nxt = G + int64_t(__shfl_sync(0xffffffffu, claim, 0));
+        uint32_t rec_nxt = 0;
+        if (nxt < n_items) {
+            rec_nxt = load_rec(nxt);
+            if (lane == 0) claim = atomicAdd(&ctr->next, 1u);
+        }
+        if (cur >= n_items || timed_out) break;
+
+        ItemMeta m;
+        if (item_meta<OP>(a, h, rec_cur, m)) {
+            for (int p = 0; p < planes && !timed_out; ++p) {
+                for (int s0 = 0; s0 < m.n_valid && !timed_out; s0 += max_rows) {
+                    const int ns = m.n_valid - s0 < max_rows ? m.n_valid - s0 : max_rows;
                     // make room: keep at most kLookahead segments in flight
                     if (issued - retired >= kLookahead) {
                         retire();
@@ -404,8 +383,8 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
                     const uint32_t bytes = uint32_t(ns) * uint32_t(row_bytes);
                     if (lane == 0) {
                         StageInfo si;
-                        si.dst = m.dst + p * m.dst_pstride + s0 * int64_t(row_bytes);
-                        si.dst2 = (OP == OP_MERGE && m.dst2) ? m.dst2 + s0 * R + int64_t(p) * a.Rp
+                        si.dst = m.dst + p * m.dst_pstride + int64_t(s0) * row_bytes;
+                        si.dst2 = (OP == OP_MERGE && m.dst2) ? m.dst2 + int64_t(s0) * R + int64_t(p) * a.Rp
                                                              : nullptr;
                         si.bytes = bytes;
                         si.rows = uint32_t(ns);
@@ -415,7 +394,7 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
                     __syncwarp();
                     if (OP == OP_GATHER || OP == OP_SCATTER) {
                         if (lane == 0)
-                            bulk_load(sbase, m.src_a + p * m.src_pstride + s0 * int64_t(row_bytes), bytes, bar);
+                            bulk_load(sbase, m.src_a + p * m.src_pstride + int64_t(s0) * row_bytes, bytes, bar);
                     } else {
                         for (int i = lane; i < ns; i += 32) {
                             const int64_t s = s0 + i;
@@ -429,6 +408,8 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
                 }
             }
         }
+        cur = nxt;
+        rec_cur = rec_nxt;
     }
     while (retired < issued && !timed_out) retire();
 
@@ -440,8 +421,14 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
     }
     bulk_wait_all();
     __syncwarp();
-    if (lane == 0)
+    if (lane == 0) {
         for (int s = 0; s < kStages; ++s) mbar_inval(bar0 + 8 * s);
+        // the last CTA of this launch resets the counter for the next launch
+        if (atomicAdd(&ctr->done, 1u) == uint32_t(G) - 1u) {
+            atomicExch(&ctr->next, 0u);
+            atomicExch(&ctr->done, 0u);
+        }
+    }
 }
 
 // One kernel per op, so launch lists and profiles name the op.
@@ -527,6 +514,7 @@ CopyArgs make_args(const kvl_geom *g, const void *d_plan, const kvl_request *d_r
     a.B = g->block_tokens;
     a.Rp = g->plane_row_bytes;
     a.layer = layer;
+    a.L = g->n_layers;
     a.N = g->pool_blocks;
     return a;
 }

@@ -9,7 +9,8 @@
 
 namespace kvl {
 
-constexpr uint32_t kPlanMagic = 0x4b564c31u;  // "KVL1"
+constexpr uint32_t kPlanMagic = 0x4b564c32u;  // "KVL2"
+constexpr int kOps = 4;  // slice, merge-scatter, gather, scatter-back
 constexpr int kMaxDevices = 64;
 
 // Start of a plan (the header section is padded to 256 bytes).
@@ -22,7 +23,7 @@ struct PlanHeader {
     int64_t n_tokens;            // 24: sum of T_all
     int64_t n_hit;               // 32: sum of T_hit
     int32_t scan_status;         // 40: status after the request scan (the fill reads it)
-    int32_t reserved;            // 44
+    int32_t n_layers;            // 44: L the plan was built for (sizes the counters)
     int64_t pool_blocks;         // 48: N the plan was built for
     int64_t block_tokens;        // 56: B the plan was built for
     unsigned long long detail[8];  // 64: per status code, smallest detail recorded
@@ -34,17 +35,47 @@ static_assert(sizeof(kvl_request) == 96, "kvl_request layout");
 
 __host__ __device__ inline size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// One work item resolved once by the plan (128 bytes, 32 words: a warp loads it with
+// one coalesced request, a word per lane).  Addresses are those of layer 0; a layer
+// adds l times the matching layer stride.
+struct ItemRec {
+    uint64_t hit_base;    //  0: hit_src + sb(j)*hit_block_stride (0: no hit rows)
+    int64_t hit_ts;       //  2: hit token stride
+    int64_t hit_ls;       //  4: hit layer stride
+    uint64_t miss_base;   //  6: miss row of slot 0: miss_src + (j*B - T_hit)*miss_ts
+    int64_t miss_ts;      //  8
+    int64_t miss_ls;      // 10
+    uint64_t obj_base;    // 12: objects + j*B*Rp (0: no objects)
+    int64_t obj_ps;       // 14: object plane stride, nblk*B*Rp
+    int64_t obj_ls;       // 16: object layer stride
+    int64_t hit_row;      // 18: row of hit_out holding slot 0 (hit_off[r] + j*B)
+    int64_t tok_row;      // 20: row of complete_out holding slot 0 (tok_off[r] + j*B)
+    int32_t pool_block;   // 22: table entry
+    int32_t n_hit;        // 23: slots that are hit tokens
+    int32_t n_valid;      // 24: slots that are tokens (T_all - j*B, at most B)
+    int32_t req;          // 25
+    int32_t pad[6];       // 26
+};
+static_assert(sizeof(ItemRec) == 128, "item record layout");
+
+// Work-claim counters of one (layer, op): the next item to claim and the CTAs done.
+struct ClaimCounter {
+    uint32_t next;
+    uint32_t done;
+};
+
 // Byte offsets of the plan's sections (see kvl_plan_layout).
 struct PlanLayout {
-    size_t off[8];
+    size_t off[10];
     __host__ __device__ PlanLayout() {}
 };
 
-__host__ __device__ inline PlanLayout plan_layout(int32_t n_req, int64_t pool_blocks)
+__host__ __device__ inline PlanLayout plan_layout(int32_t n_req, int64_t pool_blocks, int32_t n_layers)
 {
     PlanLayout p;
     size_t n1 = size_t(n_req < 0 ? 0 : n_req) + 1;
     size_t cap = size_t(pool_blocks < 0 ? 0 : pool_blocks);
+    size_t L = size_t(n_layers < 0 ? 0 : n_layers);
     p.off[0] = 0;
     p.off[1] = 256;
     p.off[2] = p.off[1] + round256(n1 * 8);
@@ -52,7 +83,9 @@ __host__ __device__ inline PlanLayout plan_layout(int32_t n_req, int64_t pool_bl
     p.off[4] = p.off[3] + round256(n1 * 8);
     p.off[5] = p.off[4] + round256(cap * 4);
     p.off[6] = p.off[5] + round256(cap * 4);
-    p.off[7] = p.off[6] + round256(((cap + 31) / 32) * 4);
+    p.off[7] = p.off[6] + round256(cap * sizeof(ItemRec));
+    p.off[8] = p.off[7] + round256(L * kOps * sizeof(ClaimCounter));
+    p.off[9] = p.off[8] + round256(((cap + 31) / 32) * 4);
     return p;
 }
 
@@ -64,12 +97,15 @@ struct PlanView {
     int64_t *blk_off;
     int32_t *item_req;
     int32_t *item_blk;
+    ItemRec *items;
+    ClaimCounter *counters;  // [L][kOps]
     uint32_t *bitmap;
 };
 
-__host__ __device__ inline PlanView plan_view(void *d_plan, int32_t n_req, int64_t pool_blocks)
+__host__ __device__ inline PlanView plan_view(void *d_plan, int32_t n_req, int64_t pool_blocks,
+                                              int32_t n_layers)
 {
-    PlanLayout l = plan_layout(n_req, pool_blocks);
+    PlanLayout l = plan_layout(n_req, pool_blocks, n_layers);
     char *b = static_cast<char *>(d_plan);
     PlanView v;
     v.hdr = reinterpret_cast<PlanHeader *>(b);
@@ -78,7 +114,9 @@ __host__ __device__ inline PlanView plan_view(void *d_plan, int32_t n_req, int64
     v.blk_off = reinterpret_cast<int64_t *>(b + l.off[3]);
     v.item_req = reinterpret_cast<int32_t *>(b + l.off[4]);
     v.item_blk = reinterpret_cast<int32_t *>(b + l.off[5]);
-    v.bitmap = reinterpret_cast<uint32_t *>(b + l.off[6]);
+    v.items = reinterpret_cast<ItemRec *>(b + l.off[6]);
+    v.counters = reinterpret_cast<ClaimCounter *>(b + l.off[7]);
+    v.bitmap = reinterpret_cast<uint32_t *>(b + l.off[8]);
     return v;
 }
 

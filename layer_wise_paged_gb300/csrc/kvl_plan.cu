@@ -7,8 +7,10 @@
 // CPU loads the I/O kernel once per layer, O(L) rather than O(L x blocks)).
 //
 // Two launches: a one-CTA scan (request validation, three exclusive prefix sums,
-// header, bitmap clear) and a grid-stride fill (work items, block-id range checks,
-// optional injectivity check through a bitmap with atomicOr).
+// header, claim counters and bitmap clear) and a grid-stride fill (work items,
+// block-id range checks, optional injectivity check through a bitmap with atomicOr,
+// and each item's resolved record: the layer-0 addresses and strides its rows are
+// read from and written to, so the copy kernels need one 128-byte load per item).
 #include <climits>
 #include <cstdint>
 #include <cstring>
@@ -30,6 +32,7 @@ struct PlanArgs {
     int32_t B;
     int64_t N;
     int32_t check_injective;
+    int32_t P, Rp, L;
 };
 
 // Inclusive scan of one int64 across a warp.
@@ -142,10 +145,14 @@ __global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(PlanArgs a)
         }
         h->status = code;
         h->scan_status = code;
-        h->reserved = 0;
+        h->n_layers = a.L;
         h->reqs = a.reqs;
         h->tables = a.tables;
         h->magic = kPlanMagic;
+    }
+    for (int64_t c = tid; c < int64_t(a.L) * kOps; c += kScanThreads) {
+        a.v.counters[c].next = 0u;
+        a.v.counters[c].done = 0u;
     }
     if (a.check_injective) {
         const int64_t words = (a.N + 31) / 32;
@@ -175,8 +182,9 @@ __global__ void __launch_bounds__(kFillThreads) plan_fill_kernel(PlanArgs a)
 
         const kvl_request &q = a.reqs[r];
         bool bad = false;
+        int64_t sb = j;
         if (j < ceil_div64(q.t_hit, a.B)) {
-            const int64_t sb = q.hit_src_table ? int64_t(q.hit_src_table[j]) : j;
+            sb = q.hit_src_table ? int64_t(q.hit_src_table[j]) : j;
             if (sb < 0 || sb >= q.hit_src_blocks) bad = true;
         }
         const int64_t b = a.tables[i];
@@ -190,6 +198,33 @@ __global__ void __launch_bounds__(kFillThreads) plan_fill_kernel(PlanArgs a)
             const uint32_t old = atomicOr(&a.v.bitmap[b >> 5], bit);
             if (old & bit) record_error(h, KVL_EDUP, (unsigned long long)b);
         }
+        // the item's record
+        const int64_t B = a.B, Rp = a.Rp, t0 = j * B;
+        const int64_t t_hit = q.t_hit, t_all = t_hit + q.t_miss;
+        const int64_t n_hit = t_hit - t0 < 0 ? 0 : (t_hit - t0 > B ? B : t_hit - t0);
+        const int64_t n_valid = t_all - t0 < 0 ? 0 : (t_all - t0 > B ? B : t_all - t0);
+        const int64_t nblk = a.v.blk_off[r + 1] - a.v.blk_off[r];
+        ItemRec rec;
+        rec.hit_base = n_hit > 0 ? reinterpret_cast<uint64_t>(q.hit_src) + uint64_t(sb * q.hit_block_stride)
+                                 : 0ull;
+        rec.hit_ts = q.hit_token_stride;
+        rec.hit_ls = q.hit_layer_stride;
+        rec.miss_base = n_valid > n_hit ? reinterpret_cast<uint64_t>(q.miss_src) +
+                                              uint64_t((t0 - t_hit) * q.miss_token_stride)
+                                        : 0ull;
+        rec.miss_ts = q.miss_token_stride;
+        rec.miss_ls = q.miss_layer_stride;
+        rec.obj_base = q.objects ? reinterpret_cast<uint64_t>(q.objects) + uint64_t(j * B * Rp) : 0ull;
+        rec.obj_ps = nblk * B * Rp;
+        rec.obj_ls = q.obj_layer_stride;
+        rec.hit_row = a.v.hit_off[r] + t0;
+        rec.tok_row = a.v.tok_off[r] + t0;
+        rec.pool_block = int32_t(b);
+        rec.n_hit = int32_t(n_hit);
+        rec.n_valid = int32_t(n_valid);
+        rec.req = r;
+        for (int k = 0; k < 6; ++k) rec.pad[k] = 0;
+        a.v.items[i] = rec;
     }
 }
 
@@ -198,16 +233,21 @@ __global__ void __launch_bounds__(kFillThreads) plan_fill_kernel(PlanArgs a)
 
 using namespace kvl;
 
-extern "C" size_t kvl_plan_bytes(int32_t n_req, int64_t pool_blocks)
+extern "C" size_t kvl_plan_bytes(const kvl_geom *geom, int32_t n_req)
 {
-    return plan_layout(n_req, pool_blocks).off[7];
+    if (check_geom(geom) != KVL_OK) return 0;
+    return plan_layout(n_req, geom->pool_blocks, geom->n_layers).off[9];
 }
 
-extern "C" void kvl_plan_layout(int32_t n_req, int64_t pool_blocks, size_t off[8])
+extern "C" void kvl_plan_layout(const kvl_geom *geom, int32_t n_req, size_t off[10])
 {
     if (!off) return;
-    const PlanLayout l = plan_layout(n_req, pool_blocks);
-    for (int k = 0; k < 8; ++k) off[k] = l.off[k];
+    if (check_geom(geom) != KVL_OK) {
+        for (int k = 0; k < 10; ++k) off[k] = 0;
+        return;
+    }
+    const PlanLayout l = plan_layout(n_req, geom->pool_blocks, geom->n_layers);
+    for (int k = 0; k < 10; ++k) off[k] = l.off[k];
 }
 
 extern "C" kvl_status kvl_batch_plan(const kvl_geom *geom, int32_t n_req, const kvl_request *d_reqs,
@@ -221,16 +261,19 @@ extern "C" kvl_status kvl_batch_plan(const kvl_geom *geom, int32_t n_req, const 
     if (!aligned16(d_plan) || (d_reqs && !aligned16(d_reqs)) ||
         (reinterpret_cast<uintptr_t>(d_block_tables) & 3u))
         return KVL_EALIGN;
-    if (plan_bytes < kvl_plan_bytes(n_req, geom->pool_blocks)) return KVL_EINVAL;
+    if (plan_bytes < kvl_plan_bytes(geom, n_req)) return KVL_EINVAL;
 
     PlanArgs a;
-    a.v = plan_view(d_plan, n_req, geom->pool_blocks);
+    a.v = plan_view(d_plan, n_req, geom->pool_blocks, geom->n_layers);
     a.reqs = d_reqs;
     a.tables = d_block_tables;
     a.n_req = n_req;
     a.B = geom->block_tokens;
     a.N = geom->pool_blocks;
     a.check_injective = check_injective ? 1 : 0;
+    a.P = geom->n_planes;
+    a.Rp = geom->plane_row_bytes;
+    a.L = geom->n_layers;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     plan_scan_kernel<<<1, kScanThreads, 0, s>>>(a);
     if (launch_status()) return KVL_ECUDA;
@@ -332,14 +375,14 @@ extern "C" kvl_status kvl_batch_plan_static_scratch(const kvl_geom *geom, int32_
         (reinterpret_cast<uintptr_t>(d_block_tables) & 3u))
         return KVL_EALIGN;
     // everything of the plan but its bitmap section
-    if (plan_bytes < plan_layout(n_req, geom->pool_blocks).off[6]) return KVL_EINVAL;
+    if (plan_bytes < plan_layout(n_req, geom->pool_blocks, geom->n_layers).off[8]) return KVL_EINVAL;
 
     uint32_t *bitmap = nullptr;
     const kvl_status sa = static_bitmap_address(&bitmap);
     if (sa) return sa;
 
     PlanArgs a;
-    a.v = plan_view(d_plan, n_req, geom->pool_blocks);
+    a.v = plan_view(d_plan, n_req, geom->pool_blocks, geom->n_layers);
     a.v.bitmap = bitmap;  // the scan kernel clears the words it uses on every call
     a.reqs = d_reqs;
     a.tables = d_block_tables;
@@ -347,6 +390,9 @@ extern "C" kvl_status kvl_batch_plan_static_scratch(const kvl_geom *geom, int32_
     a.B = geom->block_tokens;
     a.N = geom->pool_blocks;
     a.check_injective = check_injective ? 1 : 0;
+    a.P = geom->n_planes;
+    a.Rp = geom->plane_row_bytes;
+    a.L = geom->n_layers;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     plan_scan_kernel<<<1, kScanThreads, 0, s>>>(a);
     if (launch_status()) return KVL_ECUDA;

@@ -67,14 +67,18 @@ int main(void) {{
 
 
 def test_plan_layout_is_consistent(lib):
-    for n, N in [(0, 1), (1, 32), (16, 10625), (256, 49262), (1000, 1 << 20)]:
-        off = kvl.kvl_plan_layout(n, N)
+    for L, n, N in [(1, 0, 1), (2, 1, 32), (61, 16, 10625), (32, 256, 49262), (80, 1000, 1 << 20)]:
+        g = kvl.geom(L, 2, 16, 256, N)
+        off = kvl.kvl_plan_layout(g, n)
         assert off[0] == 0 and off[1] == 256
         assert all(o % 256 == 0 for o in off)
         assert off[2] - off[1] >= 8 * (n + 1) and off[4] - off[3] >= 8 * (n + 1)
         assert off[5] - off[4] >= 4 * N and off[6] - off[5] >= 4 * N
-        assert off[7] - off[6] >= 4 * ((N + 31) // 32)
-        assert kvl.kvl_plan_bytes(n, N) == off[7]
+        assert off[7] - off[6] >= 128 * N          # item records
+        assert off[8] - off[7] >= 8 * 4 * L        # claim counters
+        assert off[9] - off[8] >= 4 * ((N + 31) // 32)
+        assert kvl.kvl_plan_bytes(g, n) == off[9]
+    assert kvl.kvl_plan_bytes(kvl.geom(0, 2, 16, 256, 8), 1) == 0
 
 
 def test_status_strings_and_launch_counts(lib):

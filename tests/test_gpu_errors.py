@@ -107,13 +107,19 @@ def test_null_sources_are_einval():
     assert gb.status() == (kvl.KVL_EINVAL, 0)
 
 
-def test_tables_changed_after_planning_are_caught_by_the_copy_kernels():
+def test_tables_edited_after_planning_take_effect_only_through_a_new_plan():
     hb = host_buffers(SPEC)
     gb, d = device_batch(SPEC, hb)
     gb.plan()
-    assert gb.status() == (0, 0)
+    pool0 = d.pool.clone()
+    gb.merge_scatter(0, pool0)
+    # the plan resolved block ids when it was built: an edit alone changes nothing
     d.tables[6] = SPEC.n_pool + 1
-    gb.merge_scatter(0, d.pool)
+    pool1 = d.pool.clone()
+    gb.merge_scatter(0, pool1)
+    assert gb.status() == (0, 0) and torch.equal(pool0, pool1)
+    # a new plan sees the edit and refuses it
+    gb.plan()
     assert gb.status() == (kvl.KVL_ERANGE, 6)
 
 

@@ -35,7 +35,8 @@ def _lib():
 
 
 def _plan_bytes_used(plan_u8, off, n_req, n_items):
-    """The bytes of a plan that carry results: header fields, offsets, work list."""
+    """The bytes of a plan that carry results: header fields, offsets, work list,
+    item records and claim counters."""
     p = plan_u8.cpu().numpy()
     hdr = p[:144]
     return dict(
@@ -44,7 +45,9 @@ def _plan_bytes_used(plan_u8, off, n_req, n_items):
         hit_off=p[off[2]:off[2] + 8 * (n_req + 1)].copy(),
         blk_off=p[off[3]:off[3] + 8 * (n_req + 1)].copy(),
         item_req=p[off[4]:off[4] + 4 * n_items].copy(),
-        item_blk=p[off[5]:off[5] + 4 * n_items].copy())
+        item_blk=p[off[5]:off[5] + 4 * n_items].copy(),
+        records=p[off[6]:off[6] + 128 * n_items].copy(),
+        counters=p[off[7]:off[7] + 8 * 4 * SPEC.L].copy())
 
 
 def _compare_twice(tables_override=None):
@@ -59,7 +62,7 @@ def _compare_twice(tables_override=None):
     n_items = min(gb.n_items, SPEC.n_pool)
     want = _plan_bytes_used(gb.d_plan, off, gb.n_req, n_items)
 
-    small = torch.empty(off[6], dtype=torch.uint8, device="cuda")
+    small = torch.empty(off[8], dtype=torch.uint8, device="cuda")
     for call in range(2):
         small.fill_(0x5A + call)  # stale bytes must not leak into the result
         st = kvl.kvl_batch_plan_static_scratch(gb.g, gb.n_req, gb.d_reqs.data_ptr(),
