@@ -198,17 +198,18 @@ def kernel_source_hash() -> str:
 
 
 def recorded_traffic(kernel: str, workload: str):
-    """Per-launch DRAM bytes from the committed ncu record, if it was taken on this
-    kernel source (else None)."""
-    p = ROOT / "profiles" / "traffic.json"
+    """Per-launch DRAM bytes from the committed ncu record (profiles/dram_traffic.txt),
+    if it was taken on this kernel source, else None."""
+    p = ROOT / "profiles" / "dram_traffic.txt"
     try:
-        rec = json.loads(p.read_text())
-    except (OSError, ValueError):
+        lines = p.read_text().splitlines()
+    except OSError:
         return None
-    for r in rec.get("records", []):
-        if r.get("kernel") == kernel and r.get("workload") == workload and \
-                r.get("source_sha") == kernel_source_hash():
-            return r.get("dram_bytes_per_launch")
+    for line in lines:
+        f = line.split()
+        if len(f) == 4 and not line.startswith("#") and f[0] == kernel and f[1] == workload \
+                and f[2] == kernel_source_hash():
+            return int(f[3])
     return None
 
 
