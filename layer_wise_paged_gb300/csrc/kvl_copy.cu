@@ -9,10 +9,10 @@
 //
 // A CTA is one warp driving the Tensor Memory Accelerator's bulk copies, on every
 // SM of a persistent grid:
-//   * scheduling: CTA b takes item b, then claims further items one at a time from a
-//     per-(layer, op) counter in the plan (atomicAdd, issued one item ahead), so
-//     faster SMs take more items and all finish together; the last CTA to finish
-//     resets the counter for the next launch;
+//   * scheduling: CTA b takes items b and b + G, then claims further items one at a
+//     time from a per-(layer, op) counter in the plan (atomicAdd, issued one item
+//     ahead), so faster SMs take more items and all finish together; the last CTA to
+//     finish resets the counter for the next launch;
 //   * metadata: the plan resolved every item into a 128-byte record (bases and
 //     strides at layer 0, pool block id, hit / valid slot counts); the warp loads the
 //     next item's record (one word per lane) while the current item's copies run,
@@ -351,62 +351,69 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
         return __ldg(w + lane);
     };
 
-    // CTA b starts on item b; later items are claimed from the counter (its values
-    // count from the G statically placed items), one claim in flight ahead.
+    // CTA b takes items b and b + G; later items are claimed from the counter (its
+    // values count from the 2G statically placed items), one claim in flight ahead,
+    // and never waited on before it is needed.  An item's planes are copied back to
+    // back by one CTA: for the slice and merge-scatter they are the two halves of the
+    // same source token rows, which DRAM serves best close together in time.
     int64_t cur = blockIdx.x;
+    const int64_t nxt_static = blockIdx.x + G;
     uint32_t rec_cur = cur < n_items ? load_rec(cur) : 0u;
     uint32_t claim = 0;
     if (lane == 0) claim = atomicAdd(&ctr->next, 1u);
-    for (;;) {
-        const int64_t nxt = G + int64_t(__shfl_sync(0xffffffffu, claim, 0));
-        uint32_t rec_nxt = 0;
-        if (nxt < n_items) {
-            rec_nxt = load_rec(nxt);
-            if (lane == 0) claim = atomicAdd(&ctr->next, 1u);
+    for (bool first = true;; first = false) {
+        int64_t nxt;
+        if (first) {
+            nxt = nxt_static;
+        } else {
+            nxt = 2 * G + int64_t(__shfl_sync(0xffffffffu, claim, 0));
+            if (nxt < n_items && lane == 0) claim = atomicAdd(&ctr->next, 1u);
         }
+        uint32_t rec_nxt = 0;
+        if (nxt < n_items) rec_nxt = load_rec(nxt);
         if (cur >= n_items || timed_out) break;
 
         ItemMeta m;
         if (item_meta<OP>(a, h, rec_cur, m)) {
-            for (int p = 0; p < planes && !timed_out; ++p) {
-                for (int s0 = 0; s0 < m.n_valid && !timed_out; s0 += max_rows) {
-                    const int ns = m.n_valid - s0 < max_rows ? m.n_valid - s0 : max_rows;
-                    // make room: keep at most kLookahead segments in flight
-                    if (issued - retired >= kLookahead) {
-                        retire();
-                        if (timed_out) break;
-                    }
-                    const int st = int(issued % kStages);
-                    if (issued >= kStages) bulk_wait_read_all_but_one();
-                    const uint32_t sbase = smem0 + uint32_t(st) * kStageBytes;
-                    const uint32_t bar = bar0 + 8 * st;
-                    const uint32_t bytes = uint32_t(ns) * uint32_t(row_bytes);
-                    if (lane == 0) {
-                        StageInfo si;
-                        si.dst = m.dst + p * m.dst_pstride + int64_t(s0) * row_bytes;
-                        si.dst2 = (OP == OP_MERGE && m.dst2) ? m.dst2 + int64_t(s0) * R + int64_t(p) * a.Rp
-                                                             : nullptr;
-                        si.bytes = bytes;
-                        si.rows = uint32_t(ns);
-                        info[st] = si;
-                        mbar_arrive_expect_tx(bar, bytes);
-                    }
-                    __syncwarp();
-                    if (OP == OP_GATHER || OP == OP_SCATTER) {
-                        if (lane == 0)
-                            bulk_load(sbase, m.src_a + p * m.src_pstride + int64_t(s0) * row_bytes, bytes, bar);
-                    } else {
-                        for (int i = lane; i < ns; i += 32) {
-                            const int64_t s = s0 + i;
-                            const uint8_t *src = s < m.n_a ? m.src_a + s * m.a_stride
-                                                           : m.src_b + s * m.b_stride;
-                            bulk_load(sbase + uint32_t(i) * uint32_t(row_bytes),
-                                      src + int64_t(p) * m.src_pstride, uint32_t(row_bytes), bar);
-                        }
-                    }
-                    ++issued;
+          for (int p = 0; p < planes && !timed_out; ++p) {
+            for (int s0 = 0; s0 < m.n_valid && !timed_out; s0 += max_rows) {
+                const int ns = m.n_valid - s0 < max_rows ? m.n_valid - s0 : max_rows;
+                // make room: keep at most kLookahead segments in flight
+                if (issued - retired >= kLookahead) {
+                    retire();
+                    if (timed_out) break;
                 }
+                const int st = int(issued % kStages);
+                if (issued >= kStages) bulk_wait_read_all_but_one();
+                const uint32_t sbase = smem0 + uint32_t(st) * kStageBytes;
+                const uint32_t bar = bar0 + 8 * st;
+                const uint32_t bytes = uint32_t(ns) * uint32_t(row_bytes);
+                if (lane == 0) {
+                    StageInfo si;
+                    si.dst = m.dst + p * m.dst_pstride + int64_t(s0) * row_bytes;
+                    si.dst2 = (OP == OP_MERGE && m.dst2) ? m.dst2 + int64_t(s0) * R + int64_t(p) * a.Rp
+                                                         : nullptr;
+                    si.bytes = bytes;
+                    si.rows = uint32_t(ns);
+                    info[st] = si;
+                    mbar_arrive_expect_tx(bar, bytes);
+                }
+                __syncwarp();
+                if (OP == OP_GATHER || OP == OP_SCATTER) {
+                    if (lane == 0)
+                        bulk_load(sbase, m.src_a + p * m.src_pstride + int64_t(s0) * row_bytes, bytes, bar);
+                } else {
+                    for (int i = lane; i < ns; i += 32) {
+                        const int64_t s = s0 + i;
+                        const uint8_t *src = s < m.n_a ? m.src_a + s * m.a_stride
+                                                       : m.src_b + s * m.b_stride;
+                        bulk_load(sbase + uint32_t(i) * uint32_t(row_bytes),
+                                  src + int64_t(p) * m.src_pstride, uint32_t(row_bytes), bar);
+                    }
+                }
+                ++issued;
             }
+          }
         }
         cur = nxt;
         rec_cur = rec_nxt;
