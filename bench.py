@@ -69,6 +69,9 @@ def describe(spec) -> dict:
              requests=spec.n_req, T_hit=int(sum(spec.t_hit)), T_miss=int(sum(spec.t_miss)),
              pool_blocks=spec.n_pool, payload={"normal": "bf16 N(0,1)",
                                                 "uniform2": "bf16 U[-2,2]"}.get(spec.values, spec.values),
+             objects_layout={"layer": "[L][P][nblk][B][Rp]",
+                             "block": "[nblk][L][P][B][Rp] (one file of 2L objects per block)"}
+             [spec.objects],
              step="plan, then per layer slice, merge-scatter, gather, scatter-back "
                   "(each op over all layers before the next op)",
              l2="inputs larger than L2: every phase streams >= 8 GB past a 129 MB L2")
@@ -282,6 +285,8 @@ def bench_spec(args):
     spec = workloads.get_spec(args.workload)
     if args.layers:
         spec = dataclasses.replace(spec, L=min(spec.L, args.layers))
+    if args.objects != spec.objects:
+        spec = dataclasses.replace(spec, objects=args.objects)
     return spec
 
 
@@ -590,6 +595,8 @@ def parse_args(argv=None):
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.NAMES)
     p.add_argument("--layers", type=int, default=0,
                    help="use only the first N layers of the workload (small profiling case)")
+    p.add_argument("--objects", default="layer", choices=["layer", "block"],
+                   help="object layout: layer-major, or one file per block (2L objects each)")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-e2e", action="store_true")

@@ -39,9 +39,12 @@
  *       miss_src + (t - T_hit)*miss_token_stride + l*miss_layer_stride + p*Rp
  *   pool, block b, slot s:  pool + (((l*P + p)*N + b)*B + s)*Rp   ([L][P][N][B][Rp])
  *   object (l, p, j) of a request, B*Rp bytes:
- *       objects + l*obj_layer_stride + (p*nblk + j)*B*Rp
- *       (obj_layer_stride = P*nblk*B*Rp gives [L][P][nblk][B][Rp], object id
- *        (l*P + p)*nblk + j)
+ *       objects + l*obj_layer_stride + p*obj_plane_stride + j*obj_block_stride
+ *       layer-major [L][P][nblk][B][Rp] (object id (l*P + p)*nblk + j): strides
+ *         (P*nblk*B*Rp, nblk*B*Rp, B*Rp);
+ *       block-major [nblk][L][P][B][Rp], one "GPU file" per block holding its 2L
+ *         objects (Tutti 阅读笔记, 设计一 §3.1 and 伪代码 1: file offset = file id x
+ *         file stride + layer x per-layer size): strides (P*B*Rp, B*Rp, L*P*B*Rp)
  *   hit_out / complete_out: request r's token t at row hit_off[r] + t / tok_off[r] + t
  *       of R bytes ([sum T_hit][P][Rp] / [sum T_all][P][Rp], requests in order)
  *   block tables: one int32 array, request r's nblk entries at blk_off[r] (requests
@@ -113,6 +116,8 @@ typedef struct kvl_request {
     int64_t miss_layer_stride;
     void *objects;                /* this request's K/V objects (NULL if never gathered) */
     int64_t obj_layer_stride;
+    int64_t obj_plane_stride;
+    int64_t obj_block_stride;
     int32_t t_hit;
     int32_t t_miss;
 } kvl_request;

@@ -37,14 +37,15 @@ class kvl_geom(ctypes.Structure):
                 ("pool_blocks", ctypes.c_int64)]
 
 
-# struct kvl_request, 96 bytes, field for field
+# struct kvl_request, 112 bytes, field for field
 REQUEST_DTYPE = np.dtype([
     ("hit_src", np.uint64), ("hit_src_table", np.uint64), ("hit_src_blocks", np.int64),
     ("hit_block_stride", np.int64), ("hit_token_stride", np.int64),
     ("hit_layer_stride", np.int64), ("miss_src", np.uint64), ("miss_token_stride", np.int64),
     ("miss_layer_stride", np.int64), ("objects", np.uint64), ("obj_layer_stride", np.int64),
+    ("obj_plane_stride", np.int64), ("obj_block_stride", np.int64),
     ("t_hit", np.int32), ("t_miss", np.int32)])
-assert REQUEST_DTYPE.itemsize == 96
+assert REQUEST_DTYPE.itemsize == 112
 
 _lib = None
 
@@ -165,8 +166,8 @@ def pack_requests(requests, *, hit_base=0, miss_base=0, obj_base=0, src_table_ba
     """struct kvl_request array (host numpy) for requests given as byte layouts.
 
     Each request object carries t_hit, t_miss, hit_off, hit_src_blocks, the hit
-    strides, src_table_off (-1 = none), miss_off, the miss strides, obj_off and
-    obj_layer_stride; *_base are the device addresses the offsets are relative to
+    strides, src_table_off (-1 = none), miss_off, the miss strides, obj_off and the
+    object layer, plane and block strides; *_base are the device addresses the offsets are relative to
     (src_table_off counts int32 entries).  A zero base leaves that pointer NULL.
     """
     out = np.zeros(max(1, len(requests)), REQUEST_DTYPE)
@@ -184,6 +185,8 @@ def pack_requests(requests, *, hit_base=0, miss_base=0, obj_base=0, src_table_ba
         x["miss_layer_stride"] = q.miss_layer_stride
         x["objects"] = obj_base + q.obj_off if obj_base else 0
         x["obj_layer_stride"] = q.obj_layer_stride
+        x["obj_plane_stride"] = q.obj_plane_stride
+        x["obj_block_stride"] = q.obj_block_stride
         x["t_hit"] = q.t_hit
         x["t_miss"] = q.t_miss
     return out[:len(requests)] if requests else out[:0]

@@ -47,7 +47,7 @@ class Batch:
                              obj_base=_ptr(objects), src_table_base=_ptr(src_tables))
         raw = np.ascontiguousarray(host).view(np.uint8).reshape(-1)
         if raw.size == 0:
-            raw = np.zeros(96, np.uint8)
+            raw = np.zeros(112, np.uint8)
         self.d_reqs = torch.from_numpy(raw.copy()).to(self.device)
         self.plan_bytes = kvl_plan_bytes(self.g, self.n_req)
         self.d_plan = torch.zeros(self.plan_bytes, dtype=torch.uint8, device=self.device)

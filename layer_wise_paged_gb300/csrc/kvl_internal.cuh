@@ -31,7 +31,7 @@ struct PlanHeader {
     const void *tables;          // 136: the block tables the plan was built from
 };
 static_assert(sizeof(PlanHeader) == 144, "plan header layout");
-static_assert(sizeof(kvl_request) == 96, "kvl_request layout");
+static_assert(sizeof(kvl_request) == 112, "kvl_request layout");
 
 __host__ __device__ inline size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -45,8 +45,8 @@ struct ItemRec {
     uint64_t miss_base;   //  6: miss row of slot 0: miss_src + (j*B - T_hit)*miss_ts
     int64_t miss_ts;      //  8
     int64_t miss_ls;      // 10
-    uint64_t obj_base;    // 12: objects + j*B*Rp (0: no objects)
-    int64_t obj_ps;       // 14: object plane stride, nblk*B*Rp
+    uint64_t obj_base;    // 12: objects + j*obj_block_stride (0: no objects)
+    int64_t obj_ps;       // 14: object plane stride
     int64_t obj_ls;       // 16: object layer stride
     int64_t hit_row;      // 18: row of hit_out holding slot 0 (hit_off[r] + j*B)
     int64_t tok_row;      // 20: row of complete_out holding slot 0 (tok_off[r] + j*B)

@@ -59,7 +59,9 @@ __device__ int validate_request(const kvl_request &q)
     }
     if (q.t_miss > 0 && (!aligned16(q.miss_src) || (q.miss_token_stride | q.miss_layer_stride) & 15))
         return KVL_EALIGN;
-    if (q.objects && (!aligned16(q.objects) || (q.obj_layer_stride & 15))) return KVL_EALIGN;
+    if (q.objects &&
+        (!aligned16(q.objects) || ((q.obj_layer_stride | q.obj_plane_stride | q.obj_block_stride) & 15)))
+        return KVL_EALIGN;
     return KVL_OK;
 }
 
@@ -199,11 +201,10 @@ __global__ void __launch_bounds__(kFillThreads) plan_fill_kernel(PlanArgs a)
             if (old & bit) record_error(h, KVL_EDUP, (unsigned long long)b);
         }
         // the item's record
-        const int64_t B = a.B, Rp = a.Rp, t0 = j * B;
+        const int64_t B = a.B, t0 = j * B;
         const int64_t t_hit = q.t_hit, t_all = t_hit + q.t_miss;
         const int64_t n_hit = t_hit - t0 < 0 ? 0 : (t_hit - t0 > B ? B : t_hit - t0);
         const int64_t n_valid = t_all - t0 < 0 ? 0 : (t_all - t0 > B ? B : t_all - t0);
-        const int64_t nblk = a.v.blk_off[r + 1] - a.v.blk_off[r];
         ItemRec rec;
         rec.hit_base = n_hit > 0 ? reinterpret_cast<uint64_t>(q.hit_src) + uint64_t(sb * q.hit_block_stride)
                                  : 0ull;
@@ -214,8 +215,9 @@ __global__ void __launch_bounds__(kFillThreads) plan_fill_kernel(PlanArgs a)
                                         : 0ull;
         rec.miss_ts = q.miss_token_stride;
         rec.miss_ls = q.miss_layer_stride;
-        rec.obj_base = q.objects ? reinterpret_cast<uint64_t>(q.objects) + uint64_t(j * B * Rp) : 0ull;
-        rec.obj_ps = nblk * B * Rp;
+        rec.obj_base = q.objects ? reinterpret_cast<uint64_t>(q.objects) + uint64_t(j * q.obj_block_stride)
+                                 : 0ull;
+        rec.obj_ps = q.obj_plane_stride;
         rec.obj_ls = q.obj_layer_stride;
         rec.hit_row = a.v.hit_off[r] + t0;
         rec.tok_row = a.v.tok_off[r] + t0;

@@ -54,7 +54,8 @@ class _Req(ctypes.Structure):
                 ("hit_token_stride", ctypes.c_int64), ("hit_layer_stride", ctypes.c_int64),
                 ("miss_src", ctypes.c_void_p), ("miss_token_stride", ctypes.c_int64),
                 ("miss_layer_stride", ctypes.c_int64), ("objects", ctypes.c_void_p),
-                ("obj_layer_stride", ctypes.c_int64), ("t_hit", ctypes.c_int32),
+                ("obj_layer_stride", ctypes.c_int64), ("obj_plane_stride", ctypes.c_int64),
+                ("obj_block_stride", ctypes.c_int64), ("t_hit", ctypes.c_int32),
                 ("t_miss", ctypes.c_int32)]
 
 
@@ -98,7 +99,8 @@ class Batch:
     geom: object with L, P, B, Rp, n_pool.  requests: sequence of objects with the
     byte-layout attributes t_hit, t_miss, hit_off, hit_src_blocks, hit_block_stride,
     hit_token_stride, hit_layer_stride, src_table_off, miss_off, miss_token_stride,
-    miss_layer_stride, obj_off, obj_layer_stride.  hit, miss, objects: uint8 numpy
+    miss_layer_stride, obj_off, obj_layer_stride, obj_plane_stride, obj_block_stride.
+    hit, miss, objects: uint8 numpy
     buffers the offsets index; src_tables: packed int32 full-block tables or None;
     tables: packed int32 pool block tables (request order).
     """
@@ -132,6 +134,8 @@ class Batch:
             x.miss_layer_stride = int(q.miss_layer_stride)
             x.objects = _ptr(objects, int(q.obj_off)) if objects is not None and objects.size else None
             x.obj_layer_stride = int(q.obj_layer_stride)
+            x.obj_plane_stride = int(q.obj_plane_stride)
+            x.obj_block_stride = int(q.obj_block_stride)
             x.t_hit = int(q.t_hit)
             x.t_miss = int(q.t_miss)
 

@@ -34,7 +34,10 @@
  *   miss token t (T_hit <= t < T_all): miss_src + (t-T_hit)*miss_token_stride
  *        + l*miss_layer_stride + p*Rp
  *   pool block b, slot s:  pool + (((l*P + p)*N + b)*B + s)*Rp
- *   object (l, p, j):      objects + l*obj_layer_stride + (p*nblk + j)*B*Rp
+ *   object (l, p, j):      objects + l*obj_layer_stride + p*obj_plane_stride
+ *                          + j*obj_block_stride (layer-major [L][P][nblk][B][Rp], or
+ *                          block-major [nblk][L][P][B][Rp]: one GPU file per block
+ *                          holding its 2L objects, Tutti 阅读笔记 设计一 §3.1)
  *   hit_out / complete_out: row (prefix + t) of R bytes, requests packed in order
  *
  * Readings where the pages are silent: the pool is [L][P][N][B][Rp]; K is plane 0;
@@ -64,7 +67,7 @@ typedef struct {
     const uint8_t *miss_src;
     int64_t miss_token_stride, miss_layer_stride;
     uint8_t *objects;
-    int64_t obj_layer_stride;
+    int64_t obj_layer_stride, obj_plane_stride, obj_block_stride;
     int32_t t_hit, t_miss;
 } oracle_req;
 
@@ -270,7 +273,7 @@ int oracle_gather_objects(const oracle_geom *g, int32_t n_req, const oracle_req 
                 int64_t b = tables[tab0 + j];
                 if (b < 0 || b >= g->n_pool) { note(&status, OR_ERANGE); continue; }
                 uint8_t *obj = q->objects + (int64_t)layer * q->obj_layer_stride
-                             + ((int64_t)p * nblk + j) * obj_bytes;
+                             + (int64_t)p * q->obj_plane_stride + j * q->obj_block_stride;
                 memcpy(obj, pool_slot(g, (uint8_t *)pool, layer, p, b, 0), (size_t)obj_bytes);
             }
         tab0 += nblk;
@@ -293,7 +296,7 @@ int oracle_scatter_back(const oracle_geom *g, int32_t n_req, const oracle_req *r
                 int64_t b = tables[tab0 + j];
                 if (b < 0 || b >= g->n_pool) { note(&status, OR_ERANGE); continue; }
                 const uint8_t *obj = q->objects + (int64_t)layer * q->obj_layer_stride
-                                   + ((int64_t)p * nblk + j) * obj_bytes;
+                                   + (int64_t)p * q->obj_plane_stride + j * q->obj_block_stride;
                 memcpy(pool_slot(g, pool, layer, p, b, 0), obj, (size_t)obj_bytes);
             }
         tab0 += nblk;

@@ -70,7 +70,8 @@ def one_layer_problem(spec, lay, dev, layer, pool_before):
             q, hit_off=q.hit_off // L, hit_block_stride=q.hit_block_stride // L,
             hit_token_stride=q.hit_token_stride // L, hit_layer_stride=0,
             miss_off=miss_off[r], miss_token_stride=R, miss_layer_stride=0,
-            obj_off=obj_off, obj_layer_stride=0))
+            obj_off=obj_off, obj_layer_stride=0, obj_plane_stride=nblk * B * spec.Rp,
+            obj_block_stride=B * spec.Rp))
         obj_off += spec.P * nblk * B * spec.Rp
     objects = np.full(obj_off + GUARD, workloads.SENTINEL, np.uint8)
     g1 = SimpleNamespace(L=1, P=spec.P, B=B, Rp=spec.Rp, n_pool=spec.n_pool)

@@ -59,7 +59,7 @@ int main(void) {{
                    check=True)
     got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True,
                                                           text=True, check=True).stdout.splitlines())
-    assert int(got["sizeof_request"]) == kvl.REQUEST_DTYPE.itemsize == 96
+    assert int(got["sizeof_request"]) == kvl.REQUEST_DTYPE.itemsize == 112
     assert int(got["sizeof_geom"]) == ctypes.sizeof(kvl.kvl_geom)
     assert int(got["geom_pool_blocks"]) == kvl.kvl_geom.pool_blocks.offset
     for f in fields:

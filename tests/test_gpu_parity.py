@@ -121,7 +121,8 @@ def test_random_ragged_batches_bit_exact(case):
         L=int(g.integers(1, 4)), P=P, B=B, Rp=Rp, t_hit=t_hit, t_miss=t_miss,
         table=str(g.choice(["perm", "fragmented", "identity"])),
         source=str(g.choice(["contiguous", "permuted"])),
-        miss_order=str(g.choice(["layer", "token"])), seed=700 + case)
+        miss_order=str(g.choice(["layer", "token"])), seed=700 + case,
+        objects=str(g.choice(["layer", "block"])))
     run_parity(spec)
 
 
@@ -145,6 +146,12 @@ def test_scaled_workload_shapes_bit_exact(name):
 def test_without_injectivity_check_results_are_unchanged():
     spec = workloads.custom_spec(L=2, P=2, B=16, Rp=256, t_hit=[300, 5], t_miss=[20, 40])
     run_parity(spec, check_injective=False)
+
+
+def test_block_major_object_files():
+    spec = workloads.custom_spec(L=4, P=2, B=16, Rp=2048, t_hit=[700, 0, 130], t_miss=[33, 90, 0],
+                                 source="permuted", objects="block", seed=77)
+    run_parity(spec)
 
 
 def test_objects_with_zero_layer_stride():

@@ -31,11 +31,9 @@ MUTATIONS = {
         "blk_off[r + 1] = blk_off[r] + (th + tm) / B;"),
     "gather_ignores_request_table_offset": (
         "int64_t b = tables[tab0 + j];", "int64_t b = tables[j];"),
-    "objects_block_major": (
-        "uint8_t *obj = q->objects + (int64_t)layer * q->obj_layer_stride\n"
-        "                             + ((int64_t)p * nblk + j) * obj_bytes;",
-        "uint8_t *obj = q->objects + (int64_t)layer * q->obj_layer_stride\n"
-        "                             + ((int64_t)j * g->P + p) * obj_bytes;"),
+    "object_plane_term_dropped": (
+        "+ (int64_t)p * q->obj_plane_stride + j * q->obj_block_stride;",
+        "+ j * q->obj_block_stride;"),
     "source_table_ignored": (
         "int64_t blk = q->hit_src_table ? q->hit_src_table[j] : j;",
         "int64_t blk = j;"),
@@ -57,6 +55,7 @@ PIN_CALLS = [
     (pins.test_merge_scatter_places_hit_then_miss_tokens, dict(source="permuted", miss_order="layer")),
     (pins.test_slice_and_concatenate_keep_token_layer_plane_order, dict(source="permuted")),
     (pins.test_gather_objects_hold_blocks_in_table_order, {}),
+    (pins.test_block_major_objects_form_one_file_of_2L_objects_per_block, {}),
     (pins.test_identity_table_pool_is_a_reshape_of_complete_layer, {}),
     (pins.test_scatter_back_after_gather_restores_the_pool, {}),
     (pins.test_oracle_matches_brute_force, dict(case=1)),

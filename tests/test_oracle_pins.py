@@ -209,6 +209,47 @@ def test_gather_objects_hold_blocks_in_table_order(lib=None):
     assert np.all(hb.objects[hb.layout.obj_bytes:] == SENT)
 
 
+def test_block_major_objects_form_one_file_of_2L_objects_per_block(lib=None):
+    """Tutti 设计一 §3.1: one GPU file per KV block, holding 2L objects (a K and a V
+    object per layer); 伪代码 1 addresses object (file, layer) at file x file stride +
+    layer x per-layer size.  Decode every file back to (request, token, layer, plane)."""
+    spec = workloads.custom_spec(L=3, P=2, B=4, Rp=32, **RAGGED, table="perm",
+                                 source="permuted", seed=11, objects="block")
+    hb = host_buffers(spec, payload="tags")
+    b = batch_of(hb, lib)
+    for layer in range(spec.L):
+        assert b.merge_scatter(layer, hb.pool)[0] == oracle.OK
+        assert b.gather_objects(layer, hb.pool) == oracle.OK
+    sent_row = np.frombuffer(bytes([SENT]) * 16, np.int32)
+    obj_bytes = spec.B * spec.Rp
+    files = 0
+    for r, q in enumerate(hb.layout.requests):
+        th, ta = q.t_hit, q.t_hit + q.t_miss
+        nblk = -(-ta // spec.B)
+        for j in range(nblk):
+            f0 = q.obj_off + j * q.obj_block_stride
+            file_bytes = hb.objects[f0:f0 + 2 * spec.L * obj_bytes]
+            assert file_bytes.size == 2 * spec.L * obj_bytes  # 2L objects per file
+            tags, uniform = decode_rows(file_bytes, spec.Rp)
+            assert np.all(uniform)
+            tags = tags.reshape(spec.L, spec.P, spec.B, 4)
+            for l in range(spec.L):
+                for p in range(spec.P):
+                    for s_ in range(spec.B):
+                        t = j * spec.B + s_
+                        want = tag(r, t, l, p, int(t >= th)) if t < ta else sent_row
+                        assert np.array_equal(tags[l, p, s_], want)
+            files += 1
+    assert files == int(spec.nblk().sum())
+    assert np.all(hb.objects[hb.layout.obj_bytes:] == SENT)
+    # scatter-back from the files restores the pool
+    before = hb.pool.copy()
+    hb.pool[:] = SENT
+    for layer in range(spec.L):
+        assert b.scatter_back(layer, hb.pool) == oracle.OK
+    assert np.array_equal(hb.pool, before)
+
+
 # --------------------------------------------------------------------------
 # Special cases that reduce to numpy slicing
 # --------------------------------------------------------------------------

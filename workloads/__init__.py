@@ -61,6 +61,7 @@ class Spec:
     source: str = "contiguous"  # "contiguous" ([T_hit, L, P, Rp]) | "permuted" (blocks)
     miss_order: str = "layer"   # "layer" ([L, T_miss, P, Rp]) | "token" ([T_miss, L, P, Rp])
     seed: int = 0
+    objects: str = "layer"      # "layer" ([L][P][nblk][B][Rp]) | "block" ([nblk][L][P][B][Rp])
 
     @property
     def R(self) -> int:
@@ -122,11 +123,12 @@ NAMES = ("tiny", "llama3_8b_agentic", "qwen3_32b_long", "latent_batch", "many_sm
 
 
 def custom_spec(name="custom", *, L, P, B, Rp, t_hit, t_miss, n_pool=None, values="bytes",
-                table="perm", source="contiguous", miss_order="layer", seed=1) -> Spec:
+                table="perm", source="contiguous", miss_order="layer", seed=1,
+                objects="layer") -> Spec:
     """A small ad-hoc workload for tests (pool defaults to 1.5x the blocks needed)."""
     s = Spec(name, L=L, P=P, B=B, Rp=Rp, t_hit=tuple(int(x) for x in t_hit),
              t_miss=tuple(int(x) for x in t_miss), n_pool=1, values=values, table=table,
-             source=source, miss_order=miss_order, seed=seed)
+             source=source, miss_order=miss_order, seed=seed, objects=objects)
     if n_pool is None:
         n_pool = max(1, int(math.ceil(1.5 * max(1, int(s.nblk().sum())))))
     return replace(s, n_pool=int(n_pool))
@@ -192,6 +194,8 @@ class RequestLayout:
     miss_layer_stride: int
     obj_off: int
     obj_layer_stride: int
+    obj_plane_stride: int
+    obj_block_stride: int
 
 
 @dataclass
@@ -234,11 +238,22 @@ def layout(spec: Spec, *, objects_one_layer: bool = False) -> Layout:
             miss_strides = dict(miss_token_stride=R, miss_layer_stride=tm * R)
         else:
             miss_strides = dict(miss_token_stride=L * R, miss_layer_stride=R)
-        per_layer_obj = P * int(nblk[r]) * B * spec.Rp
+        nb, obj_sz = int(nblk[r]), B * spec.Rp
+        per_layer_obj = P * nb * obj_sz
         ob = per_layer_obj if objects_one_layer else L * per_layer_obj
+        if spec.objects == "layer":
+            obj_strides = dict(obj_layer_stride=per_layer_obj, obj_plane_stride=nb * obj_sz,
+                               obj_block_stride=obj_sz)
+        elif spec.objects == "block":  # one file per block holding its 2L objects
+            obj_strides = dict(obj_layer_stride=P * obj_sz, obj_plane_stride=obj_sz,
+                               obj_block_stride=(1 if objects_one_layer else L) * P * obj_sz)
+        else:
+            raise KeyError(spec.objects)
+        if objects_one_layer:
+            obj_strides["obj_layer_stride"] = 0
         out.requests.append(RequestLayout(
             t_hit=th, t_miss=tm, hit_off=hit, **rl_src, miss_off=miss, **miss_strides,
-            obj_off=obj, obj_layer_stride=0 if objects_one_layer else per_layer_obj))
+            obj_off=obj, **obj_strides))
         hit += hb
         miss += L * tm * R
         obj += ob
