@@ -365,7 +365,9 @@ def run_gpu(args):
     pool = bufs["pool"]
     # hit_layer[l] goes to a ring of HIT_RING per-layer buffers: each is rewritten only
     # after several other layers' traffic has pushed its lines out of L2
-    ring = min(spec.L, HIT_RING)
+    K = max(1, min(args.layers_per_launch, spec.L))  # layers per launch
+    groups = [(l0, min(K, spec.L - l0)) for l0 in range(0, spec.L, K)]
+    ring = min(spec.L, -(-max(HIT_RING, K) // K) * K)
     layer_hit = batch.total_hit * spec.R
     hit_out = torch.empty(max(16, ring * layer_hit), dtype=torch.uint8, device=dev)
     hit_views = [hit_out[(l % ring) * layer_hit:] for l in range(spec.L)]
@@ -381,24 +383,24 @@ def run_gpu(args):
         """One step of batch b on stream s (timing events around each kernel, or None)."""
         b.plan(stream=s)
         phases = (
-            ("slice", lambda l: b.slice_layer(l, hit_views[l], s)),
-            ("merge_scatter", lambda l: b.merge_scatter(l, pool, None, s)),
-            ("gather", lambda l: b.gather(l, pool, s)),
-            ("scatter_back", lambda l: b.scatter_back(l, pool, s)),
+            ("slice", lambda l, n: b.slice_layer(l, hit_views[l], s, layer_count=n)),
+            ("merge_scatter", lambda l, n: b.merge_scatter(l, pool, None, s, layer_count=n)),
+            ("gather", lambda l, n: b.gather(l, pool, s, layer_count=n)),
+            ("scatter_back", lambda l, n: b.scatter_back(l, pool, s, layer_count=n)),
         )
         for op, fn in phases:
-            for l in range(spec.L):
+            for gi, (l0, n) in enumerate(groups):
                 if events is not None:
-                    events[op][l][0].record(s)
-                    fn(l)
-                    events[op][l][1].record(s)
+                    events[op][gi][0].record(s)
+                    fn(l0, n)
+                    events[op][gi][1].record(s)
                 else:
-                    fn(l)
+                    fn(l0, n)
 
     def step(events=None, s=None):
         run_step(batch, s or stream, events)
 
-    launches_per_step = kvl.kvl_launches_per_call(0) + spec.L * 4
+    launches_per_step = kvl.kvl_launches_per_call(0) + len(groups) * 4
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -412,7 +414,7 @@ def run_gpu(args):
     ev = None
     graph = None
     if not args.eager and make_event() is not None:
-        ev = {op: [(make_event(), make_event()) for _ in range(spec.L)] for op in OPS}
+        ev = {op: [(make_event(), make_event()) for _ in groups] for op in OPS}
         graph = capture_step_graph(dev, stream, lambda s_: run_step(batch, s_, ev))
         for _ in range(2):
             graph.replay()
@@ -424,7 +426,7 @@ def run_gpu(args):
             graph.replay()
         else:
             evs = {op: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                        for _ in range(spec.L)] for op in OPS}
+                        for _ in groups] for op in OPS}
             step(evs)
             for op in OPS:
                 eager_ev[op].extend(evs[op])
@@ -458,16 +460,16 @@ def run_gpu(args):
         ts = [a.elapsed_time(b) / 1e3 for a, b in ev_used[op]]
         avg = sum(ts) / len(ts)
         per_op[op] = {"us_per_launch": round(avg * 1e6, 2),
-                      "gbs": round(op_bytes(spec)[op] / avg / 1e9, 1),
+                      "gbs": round(op_bytes(spec)[op] * spec.L / len(groups) / avg / 1e9, 1),
                       "total_s": sum(ts)}
     dom = max(OPS, key=lambda o: per_op[o]["total_s"])
     peak, peak_kind = hbm_peak()
     achieved = per_op[dom]["gbs"]
-    traffic = recorded_traffic(KERNEL_NAMES[dom], spec.name)
+    traffic = recorded_traffic(KERNEL_NAMES[dom], spec.name) if K == 1 else None
     roofline = {"bound": "hbm", "kernel": KERNEL_NAMES[dom] + f" ({dom})",
                 "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-                "algorithmic_bytes_per_launch": op_bytes(spec)[dom],
+                "algorithmic_bytes_per_launch": op_bytes(spec)[dom] * spec.L // len(groups),
                 "traffic": traffic}
     kernels = {op: {k: v for k, v in per_op[op].items() if k != "total_s"} for op in OPS}
 
@@ -563,7 +565,8 @@ def run_gpu(args):
 
     if rank == 0:
         cfg = describe(spec)
-        cfg.update(objects="one layer (layer stride 0)" if one_layer else "all layers",
+        cfg.update(layers_per_launch=K,
+                   objects="one layer (layer stride 0)" if one_layer else "all layers",
                    hit_layer_buffers=ring,
                    us_per_layer=round(elapsed / args.steps / spec.L * 1e6, 2),
                    launch="CUDA graph of one step, replayed per step" if graph is not None
@@ -595,6 +598,8 @@ def parse_args(argv=None):
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.NAMES)
     p.add_argument("--layers", type=int, default=0,
                    help="use only the first N layers of the workload (small profiling case)")
+    p.add_argument("--layers-per-launch", type=int, default=1,
+                   help="layers each copy launch covers (1 = the layer-wise pipeline)")
     p.add_argument("--objects", default="layer", choices=["layer", "block"],
                    help="object layout: layer-major, or one file per block (2L objects each)")
     p.add_argument("--e2e-steps", type=int, default=10)

@@ -189,36 +189,45 @@ kvl_status kvl_batch_plan_static_scratch(const kvl_geom *geom, int32_t n_req,
                                          int32_t check_injective, void *d_plan, size_t plan_bytes,
                                          void *stream);
 
+/* The copy calls below work on the layers [layer, layer + layer_count) in one launch:
+ * layer_count = 1 is the layer-wise pipeline of the pages (one launch per layer, as
+ * soon as that layer's data exists); a larger count serves callers that have several
+ * layers ready, e.g. restoring a whole prefix (Tutti 阅读笔记, 伪代码 1 and its note:
+ * the I/O kernel is loaded once per layer, O(L) launches, not O(L x blocks)).
+ * layer >= 0, layer_count >= 1, layer + layer_count <= L, pool_blocks * layer_count
+ * < 2^31; otherwise KVL_EINVAL. */
+
 /* kvl_slice_layer -- hit_layer[l] = hit_full_block[:, l] for every request
  * (DualPath KV Loading, "Dual-Path Loading": objects table and the slice_layer step
- * of pe_read_path / de_read_path).  Writes sum(T_hit) rows of R bytes to d_hit_out
- * (device, caller-owned, request r's rows from hit_off[r]). */
+ * of pe_read_path / de_read_path).  Writes, for each layer of the launch, sum(T_hit)
+ * rows of R bytes to d_hit_out (device, caller-owned): launch layer i (= l - layer) at
+ * row i*sum(T_hit) + hit_off[r] + t. */
 kvl_status kvl_slice_layer(const kvl_geom *geom, const void *d_plan, const kvl_request *d_reqs,
-                           int32_t layer, void *d_hit_out, void *stream);
+                           int32_t layer, int32_t layer_count, void *d_hit_out, void *stream);
 
-/* kvl_merge_scatter_paged -- slice, concatenate and scatter one layer in one pass:
+/* kvl_merge_scatter_paged -- slice, concatenate and scatter in one pass:
  * complete_layer[l] = hit_layer[l] rows then miss_layer[l] rows (DualPath KV Loading,
  * pe_read_path concatenate_tokens; de_read_path merge_layer), and token t of plane p
  * goes to pool block table[t / B], slot t % B (Tutti 阅读笔记, 前置知识 3, eq. (2)).
- *   d_pool          device pool [L][P][N][B][Rp], caller-owned; slots of this layer
- *                   named by the tables are written
- *   d_complete_out  NULL, or device [sum T_all][P][Rp] that also receives
- *                   complete_layer[l] (request r's rows from tok_off[r]) */
+ *   d_pool          device pool [L][P][N][B][Rp], caller-owned; the slots of the
+ *                   launch's layers named by the tables are written
+ *   d_complete_out  NULL, or device memory that also receives complete_layer[l]:
+ *                   launch layer i at row i*sum(T_all) + tok_off[r] + t, R bytes each */
 kvl_status kvl_merge_scatter_paged(const kvl_geom *geom, const void *d_plan,
                                    const kvl_request *d_reqs, const int32_t *d_block_tables,
-                                   int32_t layer, void *d_pool, void *d_complete_out,
-                                   void *stream);
+                                   int32_t layer, int32_t layer_count, void *d_pool,
+                                   void *d_complete_out, void *stream);
 
 /* kvl_gather_layer_objects -- per-layer K/V objects <-> paged blocks.
  * direction KVL_GATHER: object (l, p, j) = pool block table[j] of plane p, layer l,
- * for every request: the 2*nblk objects of one layer ready for transfer (Tutti
+ * for every request: the 2*nblk objects of a layer ready for transfer (Tutti
  * 阅读笔记, 前置知识 5 eq. (4); the worked trace's 8,000 per-layer entries for 4,000
  * blocks).  direction KVL_SCATTER_BACK: the inverse, restoring objects into their
  * paged blocks (伪代码 1 retrieve_layer).  Each request's `objects` must be non-NULL. */
 kvl_status kvl_gather_layer_objects(const kvl_geom *geom, const void *d_plan,
                                     const kvl_request *d_reqs, const int32_t *d_block_tables,
-                                    int32_t layer, void *d_pool, int32_t direction,
-                                    void *stream);
+                                    int32_t layer, int32_t layer_count, void *d_pool,
+                                    int32_t direction, void *stream);
 
 /* kvl_read_status -- copy the plan's status word and its detail to the host.
  * Synchronises `stream` first, so it reports every call enqueued before it.

@@ -64,9 +64,9 @@ def lib():
         L.kvl_plan_layout.argtypes, L.kvl_plan_layout.restype = [gp, i32, ctypes.POINTER(sz)], None
         L.kvl_batch_plan.argtypes = [gp, i32, vp, vp, i32, vp, sz, vp]
         L.kvl_batch_plan_static_scratch.argtypes = [gp, i32, vp, vp, i32, vp, sz, vp]
-        L.kvl_slice_layer.argtypes = [gp, vp, vp, i32, vp, vp]
-        L.kvl_merge_scatter_paged.argtypes = [gp, vp, vp, vp, i32, vp, vp, vp]
-        L.kvl_gather_layer_objects.argtypes = [gp, vp, vp, vp, i32, vp, i32, vp]
+        L.kvl_slice_layer.argtypes = [gp, vp, vp, i32, i32, vp, vp]
+        L.kvl_merge_scatter_paged.argtypes = [gp, vp, vp, vp, i32, i32, vp, vp, vp]
+        L.kvl_gather_layer_objects.argtypes = [gp, vp, vp, vp, i32, i32, vp, i32, vp]
         L.kvl_read_status.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i64), vp]
         L.kvl_status_string.argtypes, L.kvl_status_string.restype = [i32], ctypes.c_char_p
         L.kvl_launches_per_call.argtypes, L.kvl_launches_per_call.restype = [i32], i32
@@ -120,23 +120,23 @@ def kvl_batch_plan_static_scratch(g, n_req, d_reqs, d_block_tables, check_inject
 KVL_STATIC_SCRATCH_POOL_BLOCKS = 1 << 22
 
 
-def kvl_slice_layer(g, d_plan, d_reqs, layer, d_hit_out, stream=None) -> int:
-    return int(lib().kvl_slice_layer(_g(g), _p(d_plan), _p(d_reqs), int(layer), _p(d_hit_out),
-                                     _p(stream)))
+def kvl_slice_layer(g, d_plan, d_reqs, layer, layer_count, d_hit_out, stream=None) -> int:
+    return int(lib().kvl_slice_layer(_g(g), _p(d_plan), _p(d_reqs), int(layer), int(layer_count),
+                                     _p(d_hit_out), _p(stream)))
 
 
-def kvl_merge_scatter_paged(g, d_plan, d_reqs, d_block_tables, layer, d_pool,
+def kvl_merge_scatter_paged(g, d_plan, d_reqs, d_block_tables, layer, layer_count, d_pool,
                             d_complete_out=None, stream=None) -> int:
     return int(lib().kvl_merge_scatter_paged(_g(g), _p(d_plan), _p(d_reqs), _p(d_block_tables),
-                                             int(layer), _p(d_pool), _p(d_complete_out),
-                                             _p(stream)))
+                                             int(layer), int(layer_count), _p(d_pool),
+                                             _p(d_complete_out), _p(stream)))
 
 
-def kvl_gather_layer_objects(g, d_plan, d_reqs, d_block_tables, layer, d_pool, direction,
-                             stream=None) -> int:
+def kvl_gather_layer_objects(g, d_plan, d_reqs, d_block_tables, layer, layer_count, d_pool,
+                             direction, stream=None) -> int:
     return int(lib().kvl_gather_layer_objects(_g(g), _p(d_plan), _p(d_reqs), _p(d_block_tables),
-                                              int(layer), _p(d_pool), int(direction),
-                                              _p(stream)))
+                                              int(layer), int(layer_count), _p(d_pool),
+                                              int(direction), _p(stream)))
 
 
 def kvl_read_status(d_plan, stream=None):

@@ -65,6 +65,7 @@ struct CopyArgs {
     uint8_t *pool;
     uint8_t *out;  // hit_out (slice), complete_out (merge, may be null)
     int32_t P, B, Rp, layer, L;
+    int32_t layer_count;  // layers [layer, layer + layer_count) in this launch
     int64_t N;
 };
 
@@ -225,9 +226,11 @@ __device__ __forceinline__ uint64_t rec_u64(uint32_t rec, int w)
 // from the item's record.  False (after recording the error) when this op cannot
 // copy the item.
 template <int OP>
-__device__ __forceinline__ bool item_meta(const CopyArgs &a, PlanHeader *h, uint32_t rec, ItemMeta &m)
+__device__ __forceinline__ bool item_meta(const CopyArgs &a, PlanHeader *h, uint32_t rec, int64_t l,
+                                          ItemMeta &m)
 {
-    const int64_t l = a.layer, B = a.B, Rp = a.Rp;
+    const int64_t B = a.B, Rp = a.Rp;
+    const int64_t lo = l - a.layer;  // output layer within this launch
     const int64_t b = int32_t(rec_word(rec, 22));
     const int32_t n_hit = int32_t(rec_word(rec, 23));
     const int32_t n_valid = int32_t(rec_word(rec, 24));
@@ -250,7 +253,7 @@ __device__ __forceinline__ bool item_meta(const CopyArgs &a, PlanHeader *h, uint
     if (OP == OP_SLICE) {
         m.n_valid = n_hit;
         m.src_pstride = 0;
-        m.dst = a.out + hit_row * R;
+        m.dst = a.out + (lo * h->n_hit + hit_row) * R;
         m.dst_pstride = 0;
         return true;
     }
@@ -258,7 +261,7 @@ __device__ __forceinline__ bool item_meta(const CopyArgs &a, PlanHeader *h, uint
         m.src_pstride = Rp;
         m.dst = pool_blk;
         m.dst_pstride = pool_ps;
-        if (a.out) m.dst2 = a.out + tok_row * R;
+        if (a.out) m.dst2 = a.out + (lo * h->n_tokens + tok_row) * R;
         return true;
     }
     if (obj_base == 0) {
@@ -351,14 +354,16 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
         return __ldg(w + lane);
     };
 
-    // CTA b takes items b and b + G; later items are claimed from the counter (its
-    // values count from the 2G statically placed items), one claim in flight ahead,
-    // and never waited on before it is needed.  An item's planes are copied back to
-    // back by one CTA: for the slice and merge-scatter they are the two halves of the
-    // same source token rows, which DRAM serves best close together in time.
+    // Work units: (layer, item) pairs, layer by layer, over the launch's layers.  CTA b
+    // takes units b and b + G; later units are claimed from the counter (its values
+    // count from the 2G statically placed units), one claim in flight ahead, and never
+    // waited on before it is needed.  An item's planes are copied back to back by one
+    // CTA: for the slice and merge-scatter they are the two halves of the same source
+    // token rows, which DRAM serves best close together in time.
+    const int64_t n_units = n_items * a.layer_count;
     int64_t cur = blockIdx.x;
     const int64_t nxt_static = blockIdx.x + G;
-    uint32_t rec_cur = cur < n_items ? load_rec(cur) : 0u;
+    uint32_t rec_cur = cur < n_units ? load_rec(cur % n_items) : 0u;
     uint32_t claim = 0;
     if (lane == 0) claim = atomicAdd(&ctr->next, 1u);
     for (bool first = true;; first = false) {
@@ -367,14 +372,14 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
             nxt = nxt_static;
         } else {
             nxt = 2 * G + int64_t(__shfl_sync(0xffffffffu, claim, 0));
-            if (nxt < n_items && lane == 0) claim = atomicAdd(&ctr->next, 1u);
+            if (nxt < n_units && lane == 0) claim = atomicAdd(&ctr->next, 1u);
         }
         uint32_t rec_nxt = 0;
-        if (nxt < n_items) rec_nxt = load_rec(nxt);
-        if (cur >= n_items || timed_out) break;
+        if (nxt < n_units) rec_nxt = load_rec(nxt % n_items);
+        if (cur >= n_units || timed_out) break;
 
         ItemMeta m;
-        if (item_meta<OP>(a, h, rec_cur, m)) {
+        if (item_meta<OP>(a, h, rec_cur, int64_t(a.layer) + cur / n_items, m)) {
           for (int p = 0; p < planes && !timed_out; ++p) {
             for (int s0 = 0; s0 < m.n_valid && !timed_out; s0 += max_rows) {
                 const int ns = m.n_valid - s0 < max_rows ? m.n_valid - s0 : max_rows;
@@ -497,19 +502,21 @@ kvl_status launch(const CopyArgs &a, void *stream)
 }
 
 kvl_status common_checks(const kvl_geom *g, const void *d_plan, const kvl_request *d_reqs,
-                         int32_t layer, int32_t row_bytes)
+                         int32_t layer, int32_t layer_count, int32_t row_bytes)
 {
     const kvl_status s = check_geom(g);
     if (s) return s;
     if (!d_plan || !d_reqs) return KVL_EINVAL;
     if (!aligned16(d_plan) || !aligned16(d_reqs)) return KVL_EALIGN;
-    if (layer < 0 || layer >= g->n_layers) return KVL_EINVAL;
+    if (layer < 0 || layer_count < 1 || layer >= g->n_layers || layer_count > g->n_layers - layer)
+        return KVL_EINVAL;
+    if (g->pool_blocks * int64_t(layer_count) >= (int64_t(1) << 31)) return KVL_EINVAL;  // unit ids
     if (row_bytes > kStageBytes) return KVL_EINVAL;  // a row must fit one stage
     return KVL_OK;
 }
 
 CopyArgs make_args(const kvl_geom *g, const void *d_plan, const kvl_request *d_reqs,
-                   const int32_t *tables, int32_t layer, void *pool, void *out)
+                   const int32_t *tables, int32_t layer, int32_t layer_count, void *pool, void *out)
 {
     CopyArgs a;
     a.plan = const_cast<void *>(d_plan);
@@ -521,6 +528,7 @@ CopyArgs make_args(const kvl_geom *g, const void *d_plan, const kvl_request *d_r
     a.B = g->block_tokens;
     a.Rp = g->plane_row_bytes;
     a.layer = layer;
+    a.layer_count = layer_count;
     a.L = g->n_layers;
     a.N = g->pool_blocks;
     return a;
@@ -532,43 +540,49 @@ CopyArgs make_args(const kvl_geom *g, const void *d_plan, const kvl_request *d_r
 using namespace kvl;
 
 extern "C" kvl_status kvl_slice_layer(const kvl_geom *geom, const void *d_plan,
-                                      const kvl_request *d_reqs, int32_t layer, void *d_hit_out,
-                                      void *stream)
+                                      const kvl_request *d_reqs, int32_t layer, int32_t layer_count,
+                                      void *d_hit_out, void *stream)
 {
     const int32_t rb = geom ? geom->n_planes * geom->plane_row_bytes : 0;
-    kvl_status s = common_checks(geom, d_plan, d_reqs, layer, rb);
+    kvl_status s = common_checks(geom, d_plan, d_reqs, layer, layer_count, rb);
     if (s) return s;
     if (!d_hit_out) return KVL_EINVAL;
     if (!aligned16(d_hit_out)) return KVL_EALIGN;
-    return launch<OP_SLICE>(make_args(geom, d_plan, d_reqs, nullptr, layer, nullptr, d_hit_out),
-                            stream);
+    return launch<OP_SLICE>(
+        make_args(geom, d_plan, d_reqs, nullptr, layer, layer_count, nullptr, d_hit_out), stream);
 }
 
 extern "C" kvl_status kvl_merge_scatter_paged(const kvl_geom *geom, const void *d_plan,
                                               const kvl_request *d_reqs,
                                               const int32_t *d_block_tables, int32_t layer,
-                                              void *d_pool, void *d_complete_out, void *stream)
+                                              int32_t layer_count, void *d_pool,
+                                              void *d_complete_out, void *stream)
 {
-    kvl_status s = common_checks(geom, d_plan, d_reqs, layer, geom ? geom->plane_row_bytes : 0);
+    kvl_status s = common_checks(geom, d_plan, d_reqs, layer, layer_count,
+                                 geom ? geom->plane_row_bytes : 0);
     if (s) return s;
     if (!d_block_tables || !d_pool) return KVL_EINVAL;
     if ((reinterpret_cast<uintptr_t>(d_block_tables) & 3u) || !aligned16(d_pool) ||
         (d_complete_out && !aligned16(d_complete_out)))
         return KVL_EALIGN;
-    return launch<OP_MERGE>(
-        make_args(geom, d_plan, d_reqs, d_block_tables, layer, d_pool, d_complete_out), stream);
+    return launch<OP_MERGE>(make_args(geom, d_plan, d_reqs, d_block_tables, layer, layer_count,
+                                      d_pool, d_complete_out),
+                            stream);
 }
 
 extern "C" kvl_status kvl_gather_layer_objects(const kvl_geom *geom, const void *d_plan,
                                                const kvl_request *d_reqs,
                                                const int32_t *d_block_tables, int32_t layer,
-                                               void *d_pool, int32_t direction, void *stream)
+                                               int32_t layer_count, void *d_pool, int32_t direction,
+                                               void *stream)
 {
-    kvl_status s = common_checks(geom, d_plan, d_reqs, layer, geom ? geom->plane_row_bytes : 0);
+    kvl_status s = common_checks(geom, d_plan, d_reqs, layer, layer_count,
+                                 geom ? geom->plane_row_bytes : 0);
     if (s) return s;
     if (!d_block_tables || !d_pool) return KVL_EINVAL;
     if (direction != KVL_GATHER && direction != KVL_SCATTER_BACK) return KVL_EINVAL;
     if ((reinterpret_cast<uintptr_t>(d_block_tables) & 3u) || !aligned16(d_pool)) return KVL_EALIGN;
-    const CopyArgs a = make_args(geom, d_plan, d_reqs, d_block_tables, layer, d_pool, nullptr);
+    const CopyArgs a =
+        make_args(geom, d_plan, d_reqs, d_block_tables, layer, layer_count, d_pool, nullptr);
     return direction == KVL_GATHER ? launch<OP_GATHER>(a, stream) : launch<OP_SCATTER>(a, stream);
 }

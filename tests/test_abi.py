@@ -97,10 +97,12 @@ def test_host_checks_answer_before_any_device_work(lib):
     assert kvl.kvl_batch_plan(good, 1, fake, fake, 1, fake + 8, 1 << 20) == kvl.KVL_EALIGN
     assert kvl.kvl_batch_plan(good, 1, fake, fake, 1, fake, 16) == kvl.KVL_EINVAL
     assert kvl.kvl_batch_plan(good, -1, fake, fake, 1, fake, 1 << 20) == kvl.KVL_EINVAL
-    assert kvl.kvl_merge_scatter_paged(good, fake, fake, fake, 2, fake) == kvl.KVL_EINVAL
-    assert kvl.kvl_merge_scatter_paged(good, fake, fake, fake, 0, fake + 4) == kvl.KVL_EALIGN
-    assert kvl.kvl_gather_layer_objects(good, fake, fake, fake, 0, fake, 7) == kvl.KVL_EINVAL
-    assert kvl.kvl_slice_layer(good, fake, fake, 0, 0) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(good, fake, fake, fake, 2, 1, fake) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(good, fake, fake, fake, 0, 1, fake + 4) == kvl.KVL_EALIGN
+    assert kvl.kvl_merge_scatter_paged(good, fake, fake, fake, 0, 0, fake) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(good, fake, fake, fake, 1, 2, fake) == kvl.KVL_EINVAL
+    assert kvl.kvl_gather_layer_objects(good, fake, fake, fake, 0, 1, fake, 7) == kvl.KVL_EINVAL
+    assert kvl.kvl_slice_layer(good, fake, fake, 0, 1, 0) == kvl.KVL_EINVAL
     assert kvl.lib().kvl_read_status(None, None, None, None) == kvl.KVL_EINVAL
 
 

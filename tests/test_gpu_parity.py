@@ -154,6 +154,42 @@ def test_block_major_object_files():
     run_parity(spec)
 
 
+@pytest.mark.parametrize("layers", [(0, 4), (1, 2), (3, 1)])
+def test_multi_layer_launches_equal_the_layer_by_layer_oracle(layers):
+    first, count = layers
+    spec = workloads.custom_spec(L=4, P=2, B=16, Rp=256, t_hit=[300, 0, 77, 41],
+                                 t_miss=[20, 33, 0, 5], source="permuted", seed=91,
+                                 objects="block")
+    hb = host_buffers(spec)
+    gb, d = device_batch(spec, hb)
+    ob = oracle_batch(spec, hb)
+    gb.plan()
+    R = spec.R
+    n_hit, n_tok = ob.total_hit() * R, ob.total_tokens() * R
+    hit_out = sentinel_dev(count * n_hit)
+    complete = sentinel_dev(count * n_tok)
+    gb.slice_layer(first, hit_out, layer_count=count)
+    gb.merge_scatter(first, d.pool, complete, layer_count=count)
+    gb.gather(first, d.pool, layer_count=count)
+    want_hit = np.full(count * n_hit + GUARD, SENT, np.uint8)
+    want_comp = np.full(count * n_tok + GUARD, SENT, np.uint8)
+    for i, layer in enumerate(range(first, first + count)):
+        want_hit[i * n_hit:(i + 1) * n_hit] = ob.slice_layer(layer)[1]
+        want_comp[i * n_tok:(i + 1) * n_tok] = ob.merge_scatter(layer, hb.pool, want_complete=True)[1]
+        assert ob.gather_objects(layer, hb.pool) == 0
+    assert_bytes_equal(hit_out, want_hit, "hit_out")
+    assert_bytes_equal(complete, want_comp, "complete_out")
+    assert_bytes_equal(d.pool, hb.pool, "pool")
+    assert_bytes_equal(d.objects, hb.objects, "objects")
+    d.pool.fill_(SENT)
+    hb.pool[:] = SENT
+    gb.scatter_back(first, d.pool, layer_count=count)
+    for layer in range(first, first + count):
+        assert ob.scatter_back(layer, hb.pool) == 0
+    assert_bytes_equal(d.pool, hb.pool, "pool after scatter-back")
+    assert gb.status() == (0, 0)
+
+
 def test_objects_with_zero_layer_stride():
     spec = workloads.custom_spec(L=3, P=2, B=16, Rp=256, t_hit=[100, 50], t_miss=[3, 60])
     run_parity(spec, objects_one_layer=True)
