@@ -589,6 +589,101 @@ def run_gpu(args):
     return 0
 
 
+def run_overlap(args):
+    """Layer-wise pipeline under an SM budget: layer l's merge-scatter (at most k CTAs,
+    i.e. k SMs) on a transfer stream, and a synthetic compute kernel for layer l (a
+    bf16 GEMM standing in for the layer's attention) on a compute stream that waits for
+    layer l's transfer.  Transfers run ahead, so layer l+1's copy overlaps layer l's
+    compute.  For each budget: the transfer alone, the compute alone, the pipeline, and
+    the pipeline's time beyond the compute alone (bubbles plus the slowdown of sharing
+    the GPU), next to Tutti's zero-bubble condition T_transfer <= T_compute
+    (Tutti 阅读笔记, eq. (17))."""
+    import torch
+    import layer_wise_paged_gb300 as kvl
+    from layer_wise_paged_gb300.batch import Batch
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    kvl.build()
+    kvl.lib()
+    spec = bench_spec(args)
+    bufs = workloads.allocate(spec, dev)
+    lay = bufs["layout"]
+    g = (spec.L, spec.P, spec.B, spec.Rp, spec.n_pool)
+    b = Batch(g, lay.requests, bufs["hit"], bufs["miss"], bufs["objects"], bufs["tables"],
+              bufs["src_tables"])
+    pool = bufs["pool"]
+    main = torch.cuda.current_stream(dev)
+    b.plan(stream=main)
+    n = args.gemm
+    A = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    Bm = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    C = torch.empty(n, n, device=dev, dtype=torch.bfloat16)
+    xfer, comp = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    budgets = [k for k in (4, 8, 16, 32, 64, sms) if k <= sms]
+    L = spec.L
+    per_layer = op_bytes(spec)["merge_scatter"]
+
+    def timed(fn, reps=3):
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(main)
+            fn()
+            e1.record(main)
+            torch.cuda.synchronize(dev)
+            t = e0.elapsed_time(e1) / 1e3
+            best = t if best is None else min(best, t)
+        return best
+
+    def transfers(k, s):
+        for l in range(L):
+            b.merge_scatter(l, pool, None, s, max_ctas=k)
+
+    def computes(s):
+        for _ in range(L):
+            with torch.cuda.stream(s):
+                torch.matmul(A, Bm, out=C)
+
+    t_c = timed(lambda: computes(main)) / L
+    rows = []
+    for k in budgets:
+        t_r = timed(lambda: transfers(k, main)) / L
+
+        def pipeline():
+            xfer.wait_stream(main)
+            comp.wait_stream(main)
+            evs = [torch.cuda.Event() for _ in range(L)]
+            for l in range(L):
+                b.merge_scatter(l, pool, None, xfer, max_ctas=k)
+                evs[l].record(xfer)
+            for l in range(L):
+                comp.wait_event(evs[l])
+                with torch.cuda.stream(comp):
+                    torch.matmul(A, Bm, out=C)
+            main.wait_stream(xfer)
+            main.wait_stream(comp)
+        t_p = timed(pipeline) / L
+        rows.append({"sm_budget": k, "transfer_us_alone": round(t_r * 1e6, 1),
+                     "transfer_gbs_alone": round(per_layer / t_r / 1e9, 1),
+                     "compute_us_alone": round(t_c * 1e6, 1),
+                     "pipeline_us_per_layer": round(t_p * 1e6, 1),
+                     "over_compute_frac": round(max(0.0, (t_p - t_c) / t_p), 4),
+                     "zero_bubble_alone": bool(t_r <= t_c)})
+    code, detail = b.status(main)
+    if code != 0:
+        raise SystemExit(f"bench.py: status {code} detail {detail}")
+    print(json.dumps({"metric": "layer-wise overlap of merge-scatter with compute under an SM budget",
+                      "workload": spec.name, "L": L, "gemm": f"bf16 {n}x{n}x{n} per layer",
+                      "transfer": "kvl_merge_scatter_paged per layer, at most sm_budget CTAs",
+                      "rows": rows}), flush=True)
+    return 0
+
+
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -602,6 +697,9 @@ def parse_args(argv=None):
                    help="layers each copy launch covers (1 = the layer-wise pipeline)")
     p.add_argument("--objects", default="layer", choices=["layer", "block"],
                    help="object layout: layer-major, or one file per block (2L objects each)")
+    p.add_argument("--overlap", action="store_true",
+                   help="measure the layer-wise pipeline with compute under SM budgets")
+    p.add_argument("--gemm", type=int, default=4096, help="GEMM size of the --overlap compute")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-e2e", action="store_true")
@@ -618,6 +716,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.overlap:
+        return run_overlap(args)
     return run_gpu(args)
 
 

@@ -102,6 +102,15 @@ typedef struct kvl_geom {
     int64_t pool_blocks;     /* N: physical blocks in the pool */
 } kvl_geom;
 
+/* Launch options of a copy call (host memory; NULL = defaults). */
+typedef struct kvl_launch {
+    int32_t max_ctas; /* 0: one CTA on every SM (the whole GPU); k > 0: at most k CTAs,
+                         i.e. the copy occupies at most k SMs and leaves the rest to
+                         concurrent work (an I/O SM budget, as Tutti 阅读笔记 设计二
+                         gives its I/O kernels a fixed SM partition) */
+    int32_t reserved; /* must be 0 */
+} kvl_launch;
+
 /* One request (device memory: the calls take an array of these in device memory).
  * All strides are in bytes. */
 typedef struct kvl_request {
@@ -195,7 +204,8 @@ kvl_status kvl_batch_plan_static_scratch(const kvl_geom *geom, int32_t n_req,
  * layers ready, e.g. restoring a whole prefix (Tutti 阅读笔记, 伪代码 1 and its note:
  * the I/O kernel is loaded once per layer, O(L) launches, not O(L x blocks)).
  * layer >= 0, layer_count >= 1, layer + layer_count <= L, pool_blocks * layer_count
- * < 2^31; otherwise KVL_EINVAL. */
+ * < 2^31; otherwise KVL_EINVAL.  `launch` may be NULL (the whole GPU); a negative
+ * max_ctas or a non-zero reserved field is KVL_EINVAL. */
 
 /* kvl_slice_layer -- hit_layer[l] = hit_full_block[:, l] for every request
  * (DualPath KV Loading, "Dual-Path Loading": objects table and the slice_layer step
@@ -203,7 +213,8 @@ kvl_status kvl_batch_plan_static_scratch(const kvl_geom *geom, int32_t n_req,
  * rows of R bytes to d_hit_out (device, caller-owned): launch layer i (= l - layer) at
  * row i*sum(T_hit) + hit_off[r] + t. */
 kvl_status kvl_slice_layer(const kvl_geom *geom, const void *d_plan, const kvl_request *d_reqs,
-                           int32_t layer, int32_t layer_count, void *d_hit_out, void *stream);
+                           int32_t layer, int32_t layer_count, void *d_hit_out,
+                           const kvl_launch *launch, void *stream);
 
 /* kvl_merge_scatter_paged -- slice, concatenate and scatter in one pass:
  * complete_layer[l] = hit_layer[l] rows then miss_layer[l] rows (DualPath KV Loading,
@@ -216,7 +227,7 @@ kvl_status kvl_slice_layer(const kvl_geom *geom, const void *d_plan, const kvl_r
 kvl_status kvl_merge_scatter_paged(const kvl_geom *geom, const void *d_plan,
                                    const kvl_request *d_reqs, const int32_t *d_block_tables,
                                    int32_t layer, int32_t layer_count, void *d_pool,
-                                   void *d_complete_out, void *stream);
+                                   void *d_complete_out, const kvl_launch *launch, void *stream);
 
 /* kvl_gather_layer_objects -- per-layer K/V objects <-> paged blocks.
  * direction KVL_GATHER: object (l, p, j) = pool block table[j] of plane p, layer l,
@@ -227,7 +238,7 @@ kvl_status kvl_merge_scatter_paged(const kvl_geom *geom, const void *d_plan,
 kvl_status kvl_gather_layer_objects(const kvl_geom *geom, const void *d_plan,
                                     const kvl_request *d_reqs, const int32_t *d_block_tables,
                                     int32_t layer, int32_t layer_count, void *d_pool,
-                                    int32_t direction, void *stream);
+                                    int32_t direction, const kvl_launch *launch, void *stream);
 
 /* kvl_read_status -- copy the plan's status word and its detail to the host.
  * Synchronises `stream` first, so it reports every call enqueued before it.

@@ -31,6 +31,10 @@ class KvlError(RuntimeError):
                          f"({kvl_status_string(self.code)})")
 
 
+class kvl_launch(ctypes.Structure):
+    _fields_ = [("max_ctas", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
 class kvl_geom(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int32), ("n_planes", ctypes.c_int32),
                 ("block_tokens", ctypes.c_int32), ("plane_row_bytes", ctypes.c_int32),
@@ -64,9 +68,10 @@ def lib():
         L.kvl_plan_layout.argtypes, L.kvl_plan_layout.restype = [gp, i32, ctypes.POINTER(sz)], None
         L.kvl_batch_plan.argtypes = [gp, i32, vp, vp, i32, vp, sz, vp]
         L.kvl_batch_plan_static_scratch.argtypes = [gp, i32, vp, vp, i32, vp, sz, vp]
-        L.kvl_slice_layer.argtypes = [gp, vp, vp, i32, i32, vp, vp]
-        L.kvl_merge_scatter_paged.argtypes = [gp, vp, vp, vp, i32, i32, vp, vp, vp]
-        L.kvl_gather_layer_objects.argtypes = [gp, vp, vp, vp, i32, i32, vp, i32, vp]
+        lp = ctypes.POINTER(kvl_launch)
+        L.kvl_slice_layer.argtypes = [gp, vp, vp, i32, i32, vp, lp, vp]
+        L.kvl_merge_scatter_paged.argtypes = [gp, vp, vp, vp, i32, i32, vp, vp, lp, vp]
+        L.kvl_gather_layer_objects.argtypes = [gp, vp, vp, vp, i32, i32, vp, i32, lp, vp]
         L.kvl_read_status.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i64), vp]
         L.kvl_status_string.argtypes, L.kvl_status_string.restype = [i32], ctypes.c_char_p
         L.kvl_launches_per_call.argtypes, L.kvl_launches_per_call.restype = [i32], i32
@@ -89,6 +94,15 @@ def _g(g):
 
 def _p(x):
     return None if x is None or x == 0 else ctypes.c_void_p(int(x))
+
+
+def _launch(max_ctas):
+    """Launch options (None = the whole GPU)."""
+    if max_ctas is None:
+        return None
+    if isinstance(max_ctas, kvl_launch):
+        return ctypes.byref(max_ctas)
+    return ctypes.byref(kvl_launch(int(max_ctas), 0))
 
 
 def kvl_plan_bytes(g, n_req: int) -> int:
@@ -120,23 +134,24 @@ def kvl_batch_plan_static_scratch(g, n_req, d_reqs, d_block_tables, check_inject
 KVL_STATIC_SCRATCH_POOL_BLOCKS = 1 << 22
 
 
-def kvl_slice_layer(g, d_plan, d_reqs, layer, layer_count, d_hit_out, stream=None) -> int:
+def kvl_slice_layer(g, d_plan, d_reqs, layer, layer_count, d_hit_out, max_ctas=None,
+                    stream=None) -> int:
     return int(lib().kvl_slice_layer(_g(g), _p(d_plan), _p(d_reqs), int(layer), int(layer_count),
-                                     _p(d_hit_out), _p(stream)))
+                                     _p(d_hit_out), _launch(max_ctas), _p(stream)))
 
 
 def kvl_merge_scatter_paged(g, d_plan, d_reqs, d_block_tables, layer, layer_count, d_pool,
-                            d_complete_out=None, stream=None) -> int:
+                            d_complete_out=None, max_ctas=None, stream=None) -> int:
     return int(lib().kvl_merge_scatter_paged(_g(g), _p(d_plan), _p(d_reqs), _p(d_block_tables),
                                              int(layer), int(layer_count), _p(d_pool),
-                                             _p(d_complete_out), _p(stream)))
+                                             _p(d_complete_out), _launch(max_ctas), _p(stream)))
 
 
 def kvl_gather_layer_objects(g, d_plan, d_reqs, d_block_tables, layer, layer_count, d_pool,
-                             direction, stream=None) -> int:
+                             direction, max_ctas=None, stream=None) -> int:
     return int(lib().kvl_gather_layer_objects(_g(g), _p(d_plan), _p(d_reqs), _p(d_block_tables),
                                               int(layer), int(layer_count), _p(d_pool),
-                                              int(direction), _p(stream)))
+                                              int(direction), _launch(max_ctas), _p(stream)))
 
 
 def kvl_read_status(d_plan, stream=None):
@@ -192,7 +207,7 @@ def pack_requests(requests, *, hit_base=0, miss_base=0, obj_base=0, src_table_ba
     return out[:len(requests)] if requests else out[:0]
 
 
-__all__ = ["build", "lib", "geom", "kvl_geom", "REQUEST_DTYPE", "pack_requests", "check",
+__all__ = ["build", "lib", "geom", "kvl_geom", "kvl_launch", "REQUEST_DTYPE", "pack_requests", "check",
            "KvlError", "kvl_plan_bytes", "kvl_plan_layout", "kvl_batch_plan", "kvl_batch_plan_static_scratch",
            "kvl_slice_layer",
            "kvl_merge_scatter_paged", "kvl_gather_layer_objects", "kvl_read_status",

@@ -62,25 +62,27 @@ class Batch:
                              check_injective, _ptr(self.d_plan), self.plan_bytes,
                              _stream(stream)), "kvl_batch_plan")
 
-    def slice_layer(self, layer, hit_out, stream=None, layer_count=1):
+    def slice_layer(self, layer, hit_out, stream=None, layer_count=1, max_ctas=None):
         check(kvl_slice_layer(self.g, _ptr(self.d_plan), _ptr(self.d_reqs), layer, layer_count,
-                              _ptr(hit_out), _stream(stream)), "kvl_slice_layer")
+                              _ptr(hit_out), max_ctas, _stream(stream)), "kvl_slice_layer")
 
-    def merge_scatter(self, layer, pool, complete_out=None, stream=None, layer_count=1):
+    def merge_scatter(self, layer, pool, complete_out=None, stream=None, layer_count=1,
+                      max_ctas=None):
         check(kvl_merge_scatter_paged(self.g, _ptr(self.d_plan), _ptr(self.d_reqs),
                                       _ptr(self.tables), layer, layer_count, _ptr(pool),
-                                      _ptr(complete_out), _stream(stream)),
+                                      _ptr(complete_out), max_ctas, _stream(stream)),
               "kvl_merge_scatter_paged")
 
-    def gather(self, layer, pool, stream=None, layer_count=1):
+    def gather(self, layer, pool, stream=None, layer_count=1, max_ctas=None):
         check(kvl_gather_layer_objects(self.g, _ptr(self.d_plan), _ptr(self.d_reqs),
                                        _ptr(self.tables), layer, layer_count, _ptr(pool),
-                                       KVL_GATHER, _stream(stream)), "kvl_gather_layer_objects")
+                                       KVL_GATHER, max_ctas, _stream(stream)),
+              "kvl_gather_layer_objects")
 
-    def scatter_back(self, layer, pool, stream=None, layer_count=1):
+    def scatter_back(self, layer, pool, stream=None, layer_count=1, max_ctas=None):
         check(kvl_gather_layer_objects(self.g, _ptr(self.d_plan), _ptr(self.d_reqs),
                                        _ptr(self.tables), layer, layer_count, _ptr(pool),
-                                       KVL_SCATTER_BACK, _stream(stream)),
+                                       KVL_SCATTER_BACK, max_ctas, _stream(stream)),
               "kvl_gather_layer_objects")
 
     def status(self, stream=None):

@@ -463,7 +463,7 @@ constexpr int kSmemBytes = kStages * kStageBytes;
 // Grid: kCtasPerSm CTAs on every SM; opts each kernel into its shared memory once
 // per device.
 template <int OP>
-int grid_size()
+int grid_size(const kvl_launch *opts)
 {
     static bool ready[kMaxDevices] = {false};
     int dev = 0;
@@ -474,13 +474,15 @@ int grid_size()
             return 0;
         ready[dev] = true;
     }
-    return kCtasPerSm * sm_count();
+    const int full = kCtasPerSm * sm_count();
+    if (opts && opts->max_ctas > 0 && opts->max_ctas < full) return opts->max_ctas;
+    return full;
 }
 
 template <int OP>
-kvl_status launch(const CopyArgs &a, void *stream)
+kvl_status launch(const CopyArgs &a, const kvl_launch *opts, void *stream)
 {
-    const int grid = grid_size<OP>();
+    const int grid = grid_size<OP>(opts);
     if (grid <= 0) return KVL_ECUDA;
 #if KVL_PDL
     cudaLaunchConfig_t cfg = {};
@@ -502,10 +504,12 @@ kvl_status launch(const CopyArgs &a, void *stream)
 }
 
 kvl_status common_checks(const kvl_geom *g, const void *d_plan, const kvl_request *d_reqs,
-                         int32_t layer, int32_t layer_count, int32_t row_bytes)
+                         int32_t layer, int32_t layer_count, int32_t row_bytes,
+                         const kvl_launch *opts)
 {
     const kvl_status s = check_geom(g);
     if (s) return s;
+    if (opts && (opts->max_ctas < 0 || opts->reserved != 0)) return KVL_EINVAL;
     if (!d_plan || !d_reqs) return KVL_EINVAL;
     if (!aligned16(d_plan) || !aligned16(d_reqs)) return KVL_EALIGN;
     if (layer < 0 || layer_count < 1 || layer >= g->n_layers || layer_count > g->n_layers - layer)
@@ -541,25 +545,27 @@ using namespace kvl;
 
 extern "C" kvl_status kvl_slice_layer(const kvl_geom *geom, const void *d_plan,
                                       const kvl_request *d_reqs, int32_t layer, int32_t layer_count,
-                                      void *d_hit_out, void *stream)
+                                      void *d_hit_out, const kvl_launch *opts, void *stream)
 {
     const int32_t rb = geom ? geom->n_planes * geom->plane_row_bytes : 0;
-    kvl_status s = common_checks(geom, d_plan, d_reqs, layer, layer_count, rb);
+    kvl_status s = common_checks(geom, d_plan, d_reqs, layer, layer_count, rb, opts);
     if (s) return s;
     if (!d_hit_out) return KVL_EINVAL;
     if (!aligned16(d_hit_out)) return KVL_EALIGN;
     return launch<OP_SLICE>(
-        make_args(geom, d_plan, d_reqs, nullptr, layer, layer_count, nullptr, d_hit_out), stream);
+        make_args(geom, d_plan, d_reqs, nullptr, layer, layer_count, nullptr, d_hit_out), opts,
+        stream);
 }
 
 extern "C" kvl_status kvl_merge_scatter_paged(const kvl_geom *geom, const void *d_plan,
                                               const kvl_request *d_reqs,
                                               const int32_t *d_block_tables, int32_t layer,
                                               int32_t layer_count, void *d_pool,
-                                              void *d_complete_out, void *stream)
+                                              void *d_complete_out, const kvl_launch *opts,
+                                              void *stream)
 {
     kvl_status s = common_checks(geom, d_plan, d_reqs, layer, layer_count,
-                                 geom ? geom->plane_row_bytes : 0);
+                                 geom ? geom->plane_row_bytes : 0, opts);
     if (s) return s;
     if (!d_block_tables || !d_pool) return KVL_EINVAL;
     if ((reinterpret_cast<uintptr_t>(d_block_tables) & 3u) || !aligned16(d_pool) ||
@@ -567,22 +573,23 @@ extern "C" kvl_status kvl_merge_scatter_paged(const kvl_geom *geom, const void *
         return KVL_EALIGN;
     return launch<OP_MERGE>(make_args(geom, d_plan, d_reqs, d_block_tables, layer, layer_count,
                                       d_pool, d_complete_out),
-                            stream);
+                            opts, stream);
 }
 
 extern "C" kvl_status kvl_gather_layer_objects(const kvl_geom *geom, const void *d_plan,
                                                const kvl_request *d_reqs,
                                                const int32_t *d_block_tables, int32_t layer,
                                                int32_t layer_count, void *d_pool, int32_t direction,
-                                               void *stream)
+                                               const kvl_launch *opts, void *stream)
 {
     kvl_status s = common_checks(geom, d_plan, d_reqs, layer, layer_count,
-                                 geom ? geom->plane_row_bytes : 0);
+                                 geom ? geom->plane_row_bytes : 0, opts);
     if (s) return s;
     if (!d_block_tables || !d_pool) return KVL_EINVAL;
     if (direction != KVL_GATHER && direction != KVL_SCATTER_BACK) return KVL_EINVAL;
     if ((reinterpret_cast<uintptr_t>(d_block_tables) & 3u) || !aligned16(d_pool)) return KVL_EALIGN;
     const CopyArgs a =
         make_args(geom, d_plan, d_reqs, d_block_tables, layer, layer_count, d_pool, nullptr);
-    return direction == KVL_GATHER ? launch<OP_GATHER>(a, stream) : launch<OP_SCATTER>(a, stream);
+    return direction == KVL_GATHER ? launch<OP_GATHER>(a, opts, stream)
+                                   : launch<OP_SCATTER>(a, opts, stream);
 }

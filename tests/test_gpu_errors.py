@@ -144,17 +144,21 @@ def test_host_side_checks_return_without_launching():
     g, plan, reqs, tabs = gb.g, gb.d_plan.data_ptr(), gb.d_reqs.data_ptr(), gb.tables.data_ptr()
     pool = d.pool.data_ptr()
     s = torch.cuda.current_stream().cuda_stream
-    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, SPEC.L, 1, pool, None, s) == kvl.KVL_EINVAL
-    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, -1, 1, pool, None, s) == kvl.KVL_EINVAL
-    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, SPEC.L + 1, pool, None, s) == kvl.KVL_EINVAL
-    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool + 8, None, s) == kvl.KVL_EALIGN
-    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, 0, None, s) == kvl.KVL_EINVAL
-    assert kvl.kvl_gather_layer_objects(g, plan, reqs, tabs, 0, 1, pool, 2, s) == kvl.KVL_EINVAL
-    assert kvl.kvl_slice_layer(g, plan, reqs, 0, 1, 0, s) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, SPEC.L, 1, pool, None, None, s) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, -1, 1, pool, None, None, s) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, SPEC.L + 1, pool, None, None, s) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool + 8, None, None, s) == kvl.KVL_EALIGN
+    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, 0, None, None, s) == kvl.KVL_EINVAL
+    assert kvl.kvl_gather_layer_objects(g, plan, reqs, tabs, 0, 1, pool, 2, None, s) == kvl.KVL_EINVAL
+    assert kvl.kvl_slice_layer(g, plan, reqs, 0, 1, 0, None, s) == kvl.KVL_EINVAL
     assert kvl.kvl_batch_plan(g, gb.n_req, reqs, tabs, 1, plan, gb.plan_bytes - 1, s) == kvl.KVL_EINVAL
     bad = kvl.geom(SPEC.L, SPEC.P, SPEC.B, 24, SPEC.n_pool)
-    assert kvl.kvl_merge_scatter_paged(bad, plan, reqs, tabs, 0, 1, pool, None, s) == kvl.KVL_EALIGN
+    assert kvl.kvl_merge_scatter_paged(bad, plan, reqs, tabs, 0, 1, pool, None, None, s) == kvl.KVL_EALIGN
+    # launch options: a negative CTA cap or a non-zero reserved field
+    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, -1, s) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(4, 1),
+                                       s) == kvl.KVL_EINVAL
     # a plan built for another pool size is refused on the device
     other = kvl.geom(SPEC.L, SPEC.P, SPEC.B, SPEC.Rp, SPEC.n_pool - 1)
-    assert kvl.kvl_merge_scatter_paged(other, plan, reqs, tabs, 0, 1, pool, None, s) == kvl.KVL_OK
+    assert kvl.kvl_merge_scatter_paged(other, plan, reqs, tabs, 0, 1, pool, None, None, s) == kvl.KVL_OK
     assert gb.status()[0] == kvl.KVL_EINVAL

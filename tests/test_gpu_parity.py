@@ -190,6 +190,34 @@ def test_multi_layer_launches_equal_the_layer_by_layer_oracle(layers):
     assert gb.status() == (0, 0)
 
 
+@pytest.mark.parametrize("max_ctas", [1, 3, 17])
+def test_an_sm_budget_changes_nothing_but_speed(max_ctas):
+    spec = workloads.custom_spec(L=2, P=2, B=16, Rp=512, t_hit=[900, 0, 77, 410],
+                                 t_miss=[20, 133, 0, 5], source="permuted", seed=93)
+    hb = host_buffers(spec)
+    gb, d = device_batch(spec, hb)
+    ob = oracle_batch(spec, hb)
+    gb.plan()
+    hit_out = sentinel_dev(ob.total_hit() * spec.R)
+    for layer in range(spec.L):
+        gb.slice_layer(layer, hit_out, max_ctas=max_ctas)
+        gb.merge_scatter(layer, d.pool, max_ctas=max_ctas)
+        gb.gather(layer, d.pool, max_ctas=max_ctas)
+        want_hit = ob.slice_layer(layer)[1]
+        assert ob.merge_scatter(layer, hb.pool)[0] == 0
+        assert ob.gather_objects(layer, hb.pool) == 0
+        assert_bytes_equal(hit_out[:want_hit.size], want_hit, "hit_out")
+        assert_bytes_equal(d.pool, hb.pool, "pool")
+        assert_bytes_equal(d.objects, hb.objects, "objects")
+    d.pool.fill_(SENT)
+    hb.pool[:] = SENT
+    for layer in range(spec.L):
+        gb.scatter_back(layer, d.pool, max_ctas=max_ctas)
+        assert ob.scatter_back(layer, hb.pool) == 0
+    assert_bytes_equal(d.pool, hb.pool, "pool after scatter-back")
+    assert gb.status() == (0, 0)
+
+
 def test_objects_with_zero_layer_stride():
     spec = workloads.custom_spec(L=3, P=2, B=16, Rp=256, t_hit=[100, 50], t_miss=[3, 60])
     run_parity(spec, objects_one_layer=True)
