@@ -245,6 +245,14 @@ kvl_status kvl_gather_layer_objects(const kvl_geom *geom, const void *d_plan,
  * code/detail may be NULL.  Returns KVL_ECUDA if the copy fails, else KVL_OK. */
 kvl_status kvl_read_status(const void *d_plan, int32_t *code, int64_t *detail, void *stream);
 
+/* kvl_diag_wait_timeout -- exercise the copy kernels' bounded wait.  Launches one
+ * warp that waits, with the same bounded mbarrier wait the copy kernels use, for 16
+ * bytes that nothing delivers; after limit_us microseconds (1 .. 10^7) it gives up and
+ * writes KVL_ETIMEOUT to *d_status (device int32), then releases the barrier itself.
+ * It copies nothing.  Used to check that a wait that runs out returns an error the
+ * host can read and leaves the context usable. */
+kvl_status kvl_diag_wait_timeout(int32_t limit_us, int32_t *d_status, void *stream);
+
 /* Human-readable name of a status code (static string). */
 const char *kvl_status_string(kvl_status s);
 

@@ -73,6 +73,7 @@ def lib():
         L.kvl_merge_scatter_paged.argtypes = [gp, vp, vp, vp, i32, i32, vp, vp, lp, vp]
         L.kvl_gather_layer_objects.argtypes = [gp, vp, vp, vp, i32, i32, vp, i32, lp, vp]
         L.kvl_read_status.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i64), vp]
+        L.kvl_diag_wait_timeout.argtypes, L.kvl_diag_wait_timeout.restype = [i32, vp, vp], i32
         L.kvl_status_string.argtypes, L.kvl_status_string.restype = [i32], ctypes.c_char_p
         L.kvl_launches_per_call.argtypes, L.kvl_launches_per_call.restype = [i32], i32
         for f in (L.kvl_batch_plan, L.kvl_batch_plan_static_scratch, L.kvl_slice_layer, L.kvl_merge_scatter_paged,
@@ -161,6 +162,11 @@ def kvl_read_status(d_plan, stream=None):
     if st != KVL_OK:
         raise KvlError(st, "kvl_read_status")
     return int(code.value), int(detail.value)
+
+
+def kvl_diag_wait_timeout(limit_us, d_status, stream=None) -> int:
+    """Make the copy kernels' bounded wait run out (see include/kvl.h)."""
+    return int(lib().kvl_diag_wait_timeout(int(limit_us), _p(d_status), _p(stream)))
 
 
 def kvl_status_string(code: int) -> str:

@@ -137,14 +137,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 }
 
 // Bounded wait for a phase of a stage's mbarrier; false when the limit passed.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
     return true;
+}
+
+// Complete `bytes` of an mbarrier's expected transaction count from this thread.
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void bulk_load(uint32_t dst_smem, const void *src, uint32_t bytes,
@@ -227,7 +234,7 @@ __device__ __forceinline__ uint64_t rec_u64(uint32_t rec, int w)
 // copy the item.
 template <int OP>
 __device__ __forceinline__ bool item_meta(const CopyArgs &a, PlanHeader *h, uint32_t rec, int64_t l,
-                                          ItemMeta &m)
+                                          int64_t n_hit_all, int64_t n_tok_all, ItemMeta &m)
 {
     const int64_t B = a.B, Rp = a.Rp;
     const int64_t lo = l - a.layer;  // output layer within this launch
@@ -253,7 +260,7 @@ __device__ __forceinline__ bool item_meta(const CopyArgs &a, PlanHeader *h, uint
     if (OP == OP_SLICE) {
         m.n_valid = n_hit;
         m.src_pstride = 0;
-        m.dst = a.out + (lo * h->n_hit + hit_row) * R;
+        m.dst = a.out + (lo * n_hit_all + hit_row) * R;
         m.dst_pstride = 0;
         return true;
     }
@@ -261,7 +268,7 @@ __device__ __forceinline__ bool item_meta(const CopyArgs &a, PlanHeader *h, uint
         m.src_pstride = Rp;
         m.dst = pool_blk;
         m.dst_pstride = pool_ps;
-        if (a.out) m.dst2 = a.out + (lo * h->n_tokens + tok_row) * R;
+        if (a.out) m.dst2 = a.out + (lo * n_tok_all + tok_row) * R;
         return true;
     }
     if (obj_base == 0) {
@@ -360,10 +367,20 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
     // waited on before it is needed.  An item's planes are copied back to back by one
     // CTA: for the slice and merge-scatter they are the two halves of the same source
     // token rows, which DRAM serves best close together in time.
+    // unit u = (layer a.layer + u / n_items, item u % n_items); the host keeps
+    // n_units < 2^31, so 32-bit arithmetic suffices, and a one-layer launch divides
+    // nothing
     const int64_t n_units = n_items * a.layer_count;
+    const uint32_t n_items32 = uint32_t(n_items);
+    const bool one_layer = a.layer_count == 1;
+    auto item_of = [&](int64_t u) -> int64_t { return one_layer ? u : int64_t(uint32_t(u) % n_items32); };
+    auto layer_of = [&](int64_t u) -> int64_t {
+        return int64_t(a.layer) + (one_layer ? 0 : int64_t(uint32_t(u) / n_items32));
+    };
+    const int64_t n_hit_all = h->n_hit, n_tok_all = h->n_tokens;
     int64_t cur = blockIdx.x;
     const int64_t nxt_static = blockIdx.x + G;
-    uint32_t rec_cur = cur < n_units ? load_rec(cur % n_items) : 0u;
+    uint32_t rec_cur = cur < n_units ? load_rec(item_of(cur)) : 0u;
     uint32_t claim = 0;
     if (lane == 0) claim = atomicAdd(&ctr->next, 1u);
     for (bool first = true;; first = false) {
@@ -375,11 +392,11 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
             if (nxt < n_units && lane == 0) claim = atomicAdd(&ctr->next, 1u);
         }
         uint32_t rec_nxt = 0;
-        if (nxt < n_units) rec_nxt = load_rec(nxt % n_items);
+        if (nxt < n_units) rec_nxt = load_rec(item_of(nxt));
         if (cur >= n_units || timed_out) break;
 
         ItemMeta m;
-        if (item_meta<OP>(a, h, rec_cur, int64_t(a.layer) + cur / n_items, m)) {
+        if (item_meta<OP>(a, h, rec_cur, layer_of(cur), n_hit_all, n_tok_all, m)) {
           for (int p = 0; p < planes && !timed_out; ++p) {
             for (int s0 = 0; s0 < m.n_valid && !timed_out; s0 += max_rows) {
                 const int ns = m.n_valid - s0 < max_rows ? m.n_valid - s0 : max_rows;
@@ -441,6 +458,32 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
             atomicExch(&ctr->done, 0u);
         }
     }
+}
+
+// Diagnostic: the copy kernels' bounded wait, made to run out.  The barrier expects
+// 16 bytes that no copy will deliver; after limit_ns the wait gives up and the kernel
+// records KVL_ETIMEOUT, then completes the 16 bytes itself so the barrier's phase ends
+// and it can be invalidated.  No memory is copied, nothing is left in flight.
+__global__ void __launch_bounds__(32) kvl_wait_timeout_kernel(int32_t *status,
+                                                              unsigned long long limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(b, 16);
+    }
+    __syncwarp();
+    const bool done = __all_sync(0xffffffffu, mbar_wait_bounded(b, 0, limit_ns));
+    if (threadIdx.x == 0) {
+        *status = done ? KVL_OK : KVL_ETIMEOUT;
+        if (!done) mbar_complete_tx(b, 16);
+    }
+    __syncwarp();
+    mbar_wait_bounded(b, 0, limit_ns);
+    __syncwarp();
+    if (threadIdx.x == 0) mbar_inval(b);
 }
 
 // One kernel per op, so launch lists and profiles name the op.
@@ -592,4 +635,13 @@ extern "C" kvl_status kvl_gather_layer_objects(const kvl_geom *geom, const void 
         make_args(geom, d_plan, d_reqs, d_block_tables, layer, layer_count, d_pool, nullptr);
     return direction == KVL_GATHER ? launch<OP_GATHER>(a, opts, stream)
                                    : launch<OP_SCATTER>(a, opts, stream);
+}
+
+extern "C" kvl_status kvl_diag_wait_timeout(int32_t limit_us, int32_t *d_status, void *stream)
+{
+    if (!d_status || limit_us < 1 || limit_us > 10000000) return KVL_EINVAL;
+    if (reinterpret_cast<uintptr_t>(d_status) & 3u) return KVL_EALIGN;
+    kvl_wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        d_status, static_cast<unsigned long long>(limit_us) * 1000ull);
+    return launch_status();
 }

@@ -162,3 +162,25 @@ def test_host_side_checks_return_without_launching():
     other = kvl.geom(SPEC.L, SPEC.P, SPEC.B, SPEC.Rp, SPEC.n_pool - 1)
     assert kvl.kvl_merge_scatter_paged(other, plan, reqs, tabs, 0, 1, pool, None, None, s) == kvl.KVL_OK
     assert gb.status()[0] == kvl.KVL_EINVAL
+
+
+def test_a_wait_that_runs_out_reports_a_timeout_and_the_context_survives():
+    """A bounded mbarrier wait whose bytes never arrive gives up after its limit and
+    reports KVL_ETIMEOUT; the GPU stays usable for the copies that follow."""
+    st = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    assert kvl.kvl_diag_wait_timeout(20000, st.data_ptr(), s) == kvl.KVL_OK
+    torch.cuda.synchronize()
+    assert int(st.item()) == kvl.KVL_ETIMEOUT
+    assert kvl.kvl_diag_wait_timeout(0, st.data_ptr(), s) == kvl.KVL_EINVAL
+    # the context still works: a full parity round trip afterwards
+    hb = host_buffers(SPEC)
+    gb, d = device_batch(SPEC, hb)
+    gb.plan()
+    ob = oracle.Batch(geom_of(SPEC), hb.layout.requests, hb.hit, hb.miss, hb.objects,
+                      hb.tables, hb.src_tables)
+    for layer in range(SPEC.L):
+        gb.merge_scatter(layer, d.pool)
+        assert ob.merge_scatter(layer, hb.pool)[0] == 0
+    assert np.array_equal(d.pool.cpu().numpy(), hb.pool)
+    assert gb.status() == (0, 0)
