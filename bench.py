@@ -684,6 +684,89 @@ def run_overlap(args):
     return 0
 
 
+def run_host_leg(args):
+    """DualPath's host-buffer legs on one GB300: the full prompt KV held in pinned Grace
+    memory, moved over NVLink-C2C.  Fused: merge-scatter of every layer read straight
+    from the host full block into the HBM pool (the final H2D and the paging in one
+    pass), and gather of every layer's objects straight into host memory.  Against:
+    copy-engine copies of the same bytes followed (or preceded) by the device-only op.
+    Reported as GB/s across the link and as a fraction of the copy engines' rate."""
+    import torch
+    import layer_wise_paged_gb300 as kvl
+    from layer_wise_paged_gb300.batch import Batch, MappedHost
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    kvl.build()
+    kvl.lib()
+    spec = bench_spec(args)
+    bufs = workloads.allocate(spec, dev)
+    lay = bufs["layout"]
+    g = (spec.L, spec.P, spec.B, spec.Rp, spec.n_pool)
+    main = torch.cuda.current_stream(dev)
+    hit_h, miss_h = MappedHost(bufs["hit"].numel()), MappedHost(bufs["miss"].numel())
+    obj_h = MappedHost(bufs["objects"].numel())
+    hit_h.np[:] = bufs["hit"].cpu().numpy()
+    miss_h.np[:] = bufs["miss"].cpu().numpy()
+    b_host = Batch(g, lay.requests, hit_h, miss_h, obj_h, bufs["tables"], bufs["src_tables"])
+    b_dev = Batch(g, lay.requests, bufs["hit"], bufs["miss"], bufs["objects"], bufs["tables"],
+                  bufs["src_tables"])
+    b_host.plan(stream=main)
+    b_dev.plan(stream=main)
+    pool = bufs["pool"]
+    L = spec.L
+    in_bytes = (sum(spec.t_hit) + sum(spec.t_miss)) * L * spec.R
+    obj_bytes = bufs["objects"].numel()
+    tin_h = torch.from_numpy(hit_h.np)  # host views for the copy-engine legs
+    tmiss_h = torch.from_numpy(miss_h.np)
+    tobj_h = torch.from_numpy(obj_h.np)
+
+    def timed(fn, reps=4):
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(main)
+            fn()
+            e1.record(main)
+            torch.cuda.synchronize(dev)
+            t = e0.elapsed_time(e1) / 1e3
+            best = t if best is None else min(best, t)
+        return best
+
+    H = kvl.KVL_LAUNCH_HOST_SRC
+    D = kvl.KVL_LAUNCH_HOST_DST
+    t_fused_in = timed(lambda: b_host.merge_scatter(0, pool, None, main, layer_count=L, flags=H))
+    t_ce_in = timed(lambda: (bufs["hit"].copy_(tin_h, non_blocking=True),
+                             bufs["miss"].copy_(tmiss_h, non_blocking=True)))
+    t_dev_merge = timed(lambda: b_dev.merge_scatter(0, pool, None, main, layer_count=L))
+    t_fused_out = timed(lambda: b_host.gather(0, pool, main, layer_count=L, flags=D))
+    t_dev_gather = timed(lambda: b_dev.gather(0, pool, main, layer_count=L))
+    t_ce_out = timed(lambda: tobj_h.copy_(bufs["objects"], non_blocking=True))
+    for bt in (b_host, b_dev):
+        code, detail = bt.status(main)
+        if code != 0:
+            raise SystemExit(f"bench.py: status {code} detail {detail}")
+    ce_in_gbs, ce_out_gbs = in_bytes / t_ce_in / 1e9, obj_bytes / t_ce_out / 1e9
+    print(json.dumps({
+        "metric": "host-buffer legs over NVLink-C2C (GB/s across the link)",
+        "workload": spec.name, "L": L, "link_bytes_in": in_bytes, "link_bytes_out": obj_bytes,
+        "h2d": {"fused_merge_scatter_from_host_gbs": round(in_bytes / t_fused_in / 1e9, 1),
+                "copy_engine_gbs": round(ce_in_gbs, 1),
+                "copy_engine_then_device_merge_scatter_gbs":
+                    round(in_bytes / (t_ce_in + t_dev_merge) / 1e9, 1),
+                "fused_frac_of_copy_engine": round(ce_in_gbs and (in_bytes / t_fused_in / 1e9) / ce_in_gbs, 3)},
+        "d2h": {"fused_gather_to_host_gbs": round(obj_bytes / t_fused_out / 1e9, 1),
+                "copy_engine_gbs": round(ce_out_gbs, 1),
+                "device_gather_then_copy_engine_gbs":
+                    round(obj_bytes / (t_dev_gather + t_ce_out) / 1e9, 1),
+                "fused_frac_of_copy_engine": round((obj_bytes / t_fused_out / 1e9) / ce_out_gbs, 3)},
+        "launches": "one launch of all layers per fused leg"}), flush=True)
+    return 0
+
+
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -700,6 +783,8 @@ def parse_args(argv=None):
     p.add_argument("--overlap", action="store_true",
                    help="measure the layer-wise pipeline with compute under SM budgets")
     p.add_argument("--gemm", type=int, default=4096, help="GEMM size of the --overlap compute")
+    p.add_argument("--host-leg", action="store_true",
+                   help="measure the host-buffer legs over NVLink-C2C")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-e2e", action="store_true")
@@ -718,6 +803,8 @@ def main(argv=None):
         return run_reference(args)
     if args.overlap:
         return run_overlap(args)
+    if args.host_leg:
+        return run_host_leg(args)
     return run_gpu(args)
 
 

@@ -108,8 +108,17 @@ typedef struct kvl_launch {
                          i.e. the copy occupies at most k SMs and leaves the rest to
                          concurrent work (an I/O SM budget, as Tutti 阅读笔记 设计二
                          gives its I/O kernels a fixed SM partition) */
-    int32_t reserved; /* must be 0 */
+    int32_t flags;    /* 0, KVL_LAUNCH_HOST_SRC or KVL_LAUNCH_HOST_DST (not both) */
 } kvl_launch;
+
+/* The copy's sources (resp. destinations) are pinned host memory mapped into the
+ * device address space (cudaHostAlloc / cudaHostRegister): e.g. DualPath's host
+ * buffers, the full prompt KV held in Grace memory (DualPath KV Loading, "Dual-Path
+ * Loading": pe_buffer / de_buffer and the final H2D into the HBM cache).  That side
+ * is read (written) with ordinary 16-byte SM loads (stores) over NVLink-C2C; the HBM
+ * side keeps the bulk-copy path.  Without the flag every buffer must be device memory. */
+#define KVL_LAUNCH_HOST_SRC 1
+#define KVL_LAUNCH_HOST_DST 2
 
 /* One request (device memory: the calls take an array of these in device memory).
  * All strides are in bytes. */
@@ -205,7 +214,7 @@ kvl_status kvl_batch_plan_static_scratch(const kvl_geom *geom, int32_t n_req,
  * the I/O kernel is loaded once per layer, O(L) launches, not O(L x blocks)).
  * layer >= 0, layer_count >= 1, layer + layer_count <= L, pool_blocks * layer_count
  * < 2^31; otherwise KVL_EINVAL.  `launch` may be NULL (the whole GPU); a negative
- * max_ctas or a non-zero reserved field is KVL_EINVAL. */
+ * max_ctas, an unknown flag or both host flags together is KVL_EINVAL. */
 
 /* kvl_slice_layer -- hit_layer[l] = hit_full_block[:, l] for every request
  * (DualPath KV Loading, "Dual-Path Loading": objects table and the slice_layer step

@@ -32,7 +32,10 @@ class KvlError(RuntimeError):
 
 
 class kvl_launch(ctypes.Structure):
-    _fields_ = [("max_ctas", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+    _fields_ = [("max_ctas", ctypes.c_int32), ("flags", ctypes.c_int32)]
+
+
+KVL_LAUNCH_HOST_SRC, KVL_LAUNCH_HOST_DST = 1, 2
 
 
 class kvl_geom(ctypes.Structure):
@@ -97,13 +100,13 @@ def _p(x):
     return None if x is None or x == 0 else ctypes.c_void_p(int(x))
 
 
-def _launch(max_ctas):
-    """Launch options (None = the whole GPU)."""
-    if max_ctas is None:
-        return None
+def _launch(max_ctas, flags=0):
+    """Launch options: None (whole GPU, device buffers), a CTA cap, or a kvl_launch."""
     if isinstance(max_ctas, kvl_launch):
         return ctypes.byref(max_ctas)
-    return ctypes.byref(kvl_launch(int(max_ctas), 0))
+    if max_ctas is None and not flags:
+        return None
+    return ctypes.byref(kvl_launch(int(max_ctas or 0), int(flags)))
 
 
 def kvl_plan_bytes(g, n_req: int) -> int:
@@ -213,7 +216,8 @@ def pack_requests(requests, *, hit_base=0, miss_base=0, obj_base=0, src_table_ba
     return out[:len(requests)] if requests else out[:0]
 
 
-__all__ = ["build", "lib", "geom", "kvl_geom", "kvl_launch", "REQUEST_DTYPE", "pack_requests", "check",
+__all__ = ["build", "lib", "geom", "kvl_geom", "kvl_launch", "KVL_LAUNCH_HOST_SRC",
+           "KVL_LAUNCH_HOST_DST", "REQUEST_DTYPE", "pack_requests", "check",
            "KvlError", "kvl_plan_bytes", "kvl_plan_layout", "kvl_batch_plan", "kvl_batch_plan_static_scratch",
            "kvl_slice_layer",
            "kvl_merge_scatter_paged", "kvl_gather_layer_objects", "kvl_read_status",

@@ -9,13 +9,51 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (KVL_GATHER, KVL_SCATTER_BACK, check, geom, kvl_batch_plan,
+from . import (KVL_GATHER, KVL_SCATTER_BACK, check, geom, kvl_batch_plan, kvl_launch,
                kvl_gather_layer_objects, kvl_merge_scatter_paged, kvl_plan_bytes,
                kvl_plan_layout, kvl_read_status, kvl_slice_layer, pack_requests)
 
 
 def _ptr(t):
     return 0 if t is None else t.data_ptr()
+
+
+class MappedHost:
+    """Pinned host memory mapped into the device address space (cudaHostAlloc with
+    cudaHostAllocMapped), for buffers a copy call reads or writes with the
+    KVL_LAUNCH_HOST_SRC / KVL_LAUNCH_HOST_DST flags: `.np` is the host view (uint8),
+    `data_ptr()` the device address."""
+
+    _rt = None
+
+    def __init__(self, nbytes):
+        import ctypes
+        if MappedHost._rt is None:
+            torch.cuda.init()
+            MappedHost._rt = ctypes.CDLL("libcudart.so.13")
+        rt = MappedHost._rt
+        self.nbytes = max(16, int(nbytes))
+        self._h = ctypes.c_void_p()
+        if rt.cudaHostAlloc(ctypes.byref(self._h), ctypes.c_size_t(self.nbytes),
+                            ctypes.c_uint(2)) != 0:  # cudaHostAllocMapped
+            raise MemoryError(f"cudaHostAlloc of {self.nbytes} bytes failed")
+        d = ctypes.c_void_p()
+        if rt.cudaHostGetDevicePointer(ctypes.byref(d), self._h, ctypes.c_uint(0)) != 0:
+            raise RuntimeError("cudaHostGetDevicePointer failed")
+        self._d = d.value
+        buf = (ctypes.c_uint8 * self.nbytes).from_address(self._h.value)
+        self.np = np.ctypeslib.as_array(buf)
+
+    def data_ptr(self):
+        return self._d
+
+    def __del__(self):
+        try:
+            if self._h:
+                MappedHost._rt.cudaFreeHost(self._h)
+                self._h = None
+        except Exception:
+            pass
 
 
 def _stream(stream):
@@ -56,34 +94,41 @@ class Batch:
         self.total_tokens = int(sum(q.t_hit + q.t_miss for q in self.requests))
         self.n_items = int(sum(-(-(q.t_hit + q.t_miss) // self.B) for q in self.requests))
 
+    @staticmethod
+    def _opts(max_ctas, flags):
+        if not flags:
+            return max_ctas
+        return kvl_launch(int(max_ctas or 0), int(flags))
+
     # -- steps --------------------------------------------------------------
     def plan(self, check_injective=True, stream=None):
         check(kvl_batch_plan(self.g, self.n_req, _ptr(self.d_reqs), _ptr(self.tables),
                              check_injective, _ptr(self.d_plan), self.plan_bytes,
                              _stream(stream)), "kvl_batch_plan")
 
-    def slice_layer(self, layer, hit_out, stream=None, layer_count=1, max_ctas=None):
+    def slice_layer(self, layer, hit_out, stream=None, layer_count=1, max_ctas=None, flags=0):
         check(kvl_slice_layer(self.g, _ptr(self.d_plan), _ptr(self.d_reqs), layer, layer_count,
-                              _ptr(hit_out), max_ctas, _stream(stream)), "kvl_slice_layer")
+                              _ptr(hit_out), self._opts(max_ctas, flags), _stream(stream)),
+              "kvl_slice_layer")
 
     def merge_scatter(self, layer, pool, complete_out=None, stream=None, layer_count=1,
-                      max_ctas=None):
+                      max_ctas=None, flags=0):
         check(kvl_merge_scatter_paged(self.g, _ptr(self.d_plan), _ptr(self.d_reqs),
                                       _ptr(self.tables), layer, layer_count, _ptr(pool),
-                                      _ptr(complete_out), max_ctas, _stream(stream)),
-              "kvl_merge_scatter_paged")
+                                      _ptr(complete_out), self._opts(max_ctas, flags),
+                                      _stream(stream)), "kvl_merge_scatter_paged")
 
-    def gather(self, layer, pool, stream=None, layer_count=1, max_ctas=None):
+    def gather(self, layer, pool, stream=None, layer_count=1, max_ctas=None, flags=0):
         check(kvl_gather_layer_objects(self.g, _ptr(self.d_plan), _ptr(self.d_reqs),
                                        _ptr(self.tables), layer, layer_count, _ptr(pool),
-                                       KVL_GATHER, max_ctas, _stream(stream)),
+                                       KVL_GATHER, self._opts(max_ctas, flags), _stream(stream)),
               "kvl_gather_layer_objects")
 
-    def scatter_back(self, layer, pool, stream=None, layer_count=1, max_ctas=None):
+    def scatter_back(self, layer, pool, stream=None, layer_count=1, max_ctas=None, flags=0):
         check(kvl_gather_layer_objects(self.g, _ptr(self.d_plan), _ptr(self.d_reqs),
                                        _ptr(self.tables), layer, layer_count, _ptr(pool),
-                                       KVL_SCATTER_BACK, max_ctas, _stream(stream)),
-              "kvl_gather_layer_objects")
+                                       KVL_SCATTER_BACK, self._opts(max_ctas, flags),
+                                       _stream(stream)), "kvl_gather_layer_objects")
 
     def status(self, stream=None):
         """(code, detail) of the plan after everything enqueued so far (synchronises)."""

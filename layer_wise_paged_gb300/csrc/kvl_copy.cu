@@ -66,6 +66,7 @@ struct CopyArgs {
     uint8_t *out;  // hit_out (slice), complete_out (merge, may be null)
     int32_t P, B, Rp, layer, L;
     int32_t layer_count;  // layers [layer, layer + layer_count) in this launch
+    int32_t flags;        // KVL_LAUNCH_HOST_SRC / KVL_LAUNCH_HOST_DST
     int64_t N;
 };
 
@@ -198,6 +199,85 @@ __device__ __forceinline__ void grid_dependency_wait()
 #endif
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Ordinary SM accesses, for the side of a copy that lives in pinned host memory.
+__device__ __forceinline__ uint4 ld_global_v4(const uint8_t *p)
+{
+    uint4 r;
+    asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void st_global_v4(uint8_t *p, const uint4 &v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t a)
+{
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(a));
+    return r;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t a, const uint4 &v)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// Read `nrows` rows of `row_bytes` (row r at rowptr(r)) into shared memory at
+// sbase + r*row_bytes with 16-byte loads: four rows and four vectors per lane, 8 KiB a
+// warp, in flight per round trip (NVLink-C2C round trips take microseconds).
+template <typename RowPtr>
+__device__ __forceinline__ void lsu_rows_to_smem(const RowPtr &rowptr, int nrows, int row_bytes,
+                                                 uint32_t sbase, int lane)
+{
+    constexpr int kRows = 4, kVec = 4;
+    const int vpr = row_bytes >> 4;
+    for (int r = 0; r < nrows; r += kRows) {
+        const uint8_t *p[kRows];
+#pragma unroll
+        for (int q = 0; q < kRows; ++q) p[q] = r + q < nrows ? rowptr(r + q) : nullptr;
+        for (int c0 = 0; c0 < vpr; c0 += 32 * kVec) {
+            uint4 x[kRows][kVec];
+#pragma unroll
+            for (int q = 0; q < kRows; ++q)
+#pragma unroll
+                for (int k = 0; k < kVec; ++k) {
+                    const int c = c0 + k * 32 + lane;
+                    if (p[q] && c < vpr) x[q][k] = ld_global_v4(p[q] + c * 16);
+                }
+#pragma unroll
+            for (int q = 0; q < kRows; ++q)
+#pragma unroll
+                for (int k = 0; k < kVec; ++k) {
+                    const int c = c0 + k * 32 + lane;
+                    if (p[q] && c < vpr)
+                        st_shared_v4(sbase + uint32_t(r + q) * uint32_t(row_bytes) + uint32_t(c) * 16,
+                                     x[q][k]);
+                }
+        }
+    }
+}
+
+// Write `bytes` of shared memory at `src` to global `dst` with 16-byte stores.
+__device__ __forceinline__ void lsu_smem_to_global(uint8_t *dst, uint32_t src, uint32_t bytes, int lane)
+{
+    for (uint32_t v = lane; v < bytes / 16; v += 32) st_global_v4(dst + v * 16, ld_shared_v4(src + v * 16));
+}
+
 template <typename T>
 __device__ __forceinline__ T shfl_ptr(T p, int src)
 {
@@ -301,7 +381,9 @@ struct StageInfo {
     uint32_t rows;
 };
 
-template <int OP>
+// HOST: 0 = every buffer in device memory (bulk copies both ways), 1 = sources in
+// pinned host memory (SM loads), 2 = destinations in pinned host memory (SM stores).
+template <int OP, int HOST>
 __device__ __forceinline__ void copy_rows(const CopyArgs &a)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -334,6 +416,8 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
 
     int64_t issued = 0, retired = 0;
     bool timed_out = false;
+    constexpr bool host_src = HOST == 1;
+    constexpr bool host_dst = HOST == 2;
 
     // Retire the oldest issued segment: wait for its loads, store it.
     auto retire = [&]() {
@@ -347,11 +431,23 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
         fence_proxy_async_smem();
         const StageInfo si = info[st];
         const uint32_t src = smem0 + uint32_t(st) * kStageBytes;
-        if (OP == OP_MERGE && si.dst2 != nullptr) {
-            for (uint32_t i = lane; i < si.rows; i += 32)
-                bulk_store(si.dst2 + int64_t(i) * R, src + i * uint32_t(row_bytes), uint32_t(row_bytes));
+        if constexpr (host_dst) {
+            // the destination is host memory: SM stores over NVLink-C2C
+            if (OP == OP_MERGE && si.dst2 != nullptr)
+                for (uint32_t i = 0; i < si.rows; ++i)
+                    lsu_smem_to_global(si.dst2 + int64_t(i) * R, src + i * uint32_t(row_bytes),
+                                       uint32_t(row_bytes), lane);
+            lsu_smem_to_global(si.dst, src, si.bytes, lane);
+            // the stage's generic reads come before the next bulk load into it
+            fence_proxy_async_smem();
+            __syncwarp();
+        } else {
+            if (OP == OP_MERGE && si.dst2 != nullptr) {
+                for (uint32_t i = lane; i < si.rows; i += 32)
+                    bulk_store(si.dst2 + int64_t(i) * R, src + i * uint32_t(row_bytes), uint32_t(row_bytes));
+            }
+            if (lane == 0) bulk_store(si.dst, src, si.bytes);
         }
-        if (lane == 0) bulk_store(si.dst, src, si.bytes);
         bulk_commit();
         ++retired;
     };
@@ -418,10 +514,29 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
                     si.bytes = bytes;
                     si.rows = uint32_t(ns);
                     info[st] = si;
-                    mbar_arrive_expect_tx(bar, bytes);
+                    if (!host_src) mbar_arrive_expect_tx(bar, bytes);
                 }
                 __syncwarp();
-                if (OP == OP_GATHER || OP == OP_SCATTER) {
+                if constexpr (host_src) {
+                    // the source is host memory: SM loads over NVLink-C2C into the stage
+                    if (OP == OP_GATHER || OP == OP_SCATTER) {
+                        const uint8_t *base = m.src_a + p * m.src_pstride + int64_t(s0) * row_bytes;
+                        lsu_rows_to_smem([&](int i) { return base + int64_t(i) * row_bytes; }, ns,
+                                         row_bytes, sbase, lane);
+                    } else {
+                        lsu_rows_to_smem(
+                            [&](int i) {
+                                const int64_t s = s0 + i;
+                                return (s < m.n_a ? m.src_a + s * m.a_stride : m.src_b + s * m.b_stride) +
+                                       int64_t(p) * m.src_pstride;
+                            },
+                            ns, row_bytes, sbase, lane);
+                    }
+                    // the stage's generic writes come before the bulk store that reads it
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar);
+                } else if (OP == OP_GATHER || OP == OP_SCATTER) {
                     if (lane == 0)
                         bulk_load(sbase, m.src_a + p * m.src_pstride + int64_t(s0) * row_bytes, bytes, bar);
                 } else {
@@ -486,33 +601,45 @@ __global__ void __launch_bounds__(32) kvl_wait_timeout_kernel(int32_t *status,
     if (threadIdx.x == 0) mbar_inval(b);
 }
 
-// One kernel per op, so launch lists and profiles name the op.
-__global__ void __launch_bounds__(32) kvl_slice_kernel(CopyArgs a) { copy_rows<OP_SLICE>(a); }
-__global__ void __launch_bounds__(32) kvl_merge_scatter_kernel(CopyArgs a) { copy_rows<OP_MERGE>(a); }
-__global__ void __launch_bounds__(32) kvl_gather_kernel(CopyArgs a) { copy_rows<OP_GATHER>(a); }
-__global__ void __launch_bounds__(32) kvl_scatter_back_kernel(CopyArgs a) { copy_rows<OP_SCATTER>(a); }
+// One kernel per op for device buffers, so launch lists and profiles name the op; the
+// host-memory variants are separate instantiations, so the device path carries none of
+// their code.
+__global__ void __launch_bounds__(32) kvl_slice_kernel(CopyArgs a) { copy_rows<OP_SLICE, 0>(a); }
+__global__ void __launch_bounds__(32) kvl_merge_scatter_kernel(CopyArgs a) { copy_rows<OP_MERGE, 0>(a); }
+__global__ void __launch_bounds__(32) kvl_gather_kernel(CopyArgs a) { copy_rows<OP_GATHER, 0>(a); }
+__global__ void __launch_bounds__(32) kvl_scatter_back_kernel(CopyArgs a) { copy_rows<OP_SCATTER, 0>(a); }
 
-template <int OP>
+template <int OP, int HOST>
+__global__ void __launch_bounds__(32) kvl_host_copy_kernel(CopyArgs a)
+{
+    copy_rows<OP, HOST>(a);
+}
+
+template <int OP, int HOST>
 constexpr void (*kernel_of())(CopyArgs)
 {
-    return OP == OP_SLICE ? kvl_slice_kernel
-         : OP == OP_MERGE ? kvl_merge_scatter_kernel
-         : OP == OP_GATHER ? kvl_gather_kernel
-                           : kvl_scatter_back_kernel;
+    if constexpr (HOST != 0) {
+        return kvl_host_copy_kernel<OP, HOST>;
+    } else {
+        return OP == OP_SLICE ? kvl_slice_kernel
+             : OP == OP_MERGE ? kvl_merge_scatter_kernel
+             : OP == OP_GATHER ? kvl_gather_kernel
+                               : kvl_scatter_back_kernel;
+    }
 }
 
 constexpr int kSmemBytes = kStages * kStageBytes;
 
 // Grid: kCtasPerSm CTAs on every SM; opts each kernel into its shared memory once
 // per device.
-template <int OP>
+template <int OP, int HOST>
 int grid_size(const kvl_launch *opts)
 {
     static bool ready[kMaxDevices] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
     if (!ready[dev]) {
-        if (cudaFuncSetAttribute(kernel_of<OP>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(kernel_of<OP, HOST>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBytes) != cudaSuccess)
             return 0;
         ready[dev] = true;
@@ -522,10 +649,10 @@ int grid_size(const kvl_launch *opts)
     return full;
 }
 
-template <int OP>
-kvl_status launch(const CopyArgs &a, const kvl_launch *opts, void *stream)
+template <int OP, int HOST>
+kvl_status launch_mode(const CopyArgs &a, const kvl_launch *opts, void *stream)
 {
-    const int grid = grid_size<OP>(opts);
+    const int grid = grid_size<OP, HOST>(opts);
     if (grid <= 0) return KVL_ECUDA;
 #if KVL_PDL
     cudaLaunchConfig_t cfg = {};
@@ -538,12 +665,22 @@ kvl_status launch(const CopyArgs &a, const kvl_launch *opts, void *stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kernel_of<OP>(), a) != cudaSuccess) return KVL_ECUDA;
+    if (cudaLaunchKernelEx(&cfg, kernel_of<OP, HOST>(), a) != cudaSuccess) return KVL_ECUDA;
     return KVL_OK;
 #else
-    kernel_of<OP>()<<<grid, 32, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(a);
+    kernel_of<OP, HOST>()<<<grid, 32, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(a);
     return launch_status();
 #endif
+}
+
+template <int OP>
+kvl_status launch(const CopyArgs &args, const kvl_launch *opts, void *stream)
+{
+    CopyArgs a = args;
+    a.flags = opts ? opts->flags : 0;
+    if (a.flags == KVL_LAUNCH_HOST_SRC) return launch_mode<OP, 1>(a, opts, stream);
+    if (a.flags == KVL_LAUNCH_HOST_DST) return launch_mode<OP, 2>(a, opts, stream);
+    return launch_mode<OP, 0>(a, opts, stream);
 }
 
 kvl_status common_checks(const kvl_geom *g, const void *d_plan, const kvl_request *d_reqs,
@@ -552,7 +689,9 @@ kvl_status common_checks(const kvl_geom *g, const void *d_plan, const kvl_reques
 {
     const kvl_status s = check_geom(g);
     if (s) return s;
-    if (opts && (opts->max_ctas < 0 || opts->reserved != 0)) return KVL_EINVAL;
+    if (opts && (opts->max_ctas < 0 || (opts->flags & ~(KVL_LAUNCH_HOST_SRC | KVL_LAUNCH_HOST_DST)) ||
+                 opts->flags == (KVL_LAUNCH_HOST_SRC | KVL_LAUNCH_HOST_DST)))
+        return KVL_EINVAL;
     if (!d_plan || !d_reqs) return KVL_EINVAL;
     if (!aligned16(d_plan) || !aligned16(d_reqs)) return KVL_EALIGN;
     if (layer < 0 || layer_count < 1 || layer >= g->n_layers || layer_count > g->n_layers - layer)
@@ -576,6 +715,7 @@ CopyArgs make_args(const kvl_geom *g, const void *d_plan, const kvl_request *d_r
     a.Rp = g->plane_row_bytes;
     a.layer = layer;
     a.layer_count = layer_count;
+    a.flags = 0;
     a.L = g->n_layers;
     a.N = g->pool_blocks;
     return a;

@@ -10,7 +10,14 @@ import torch
 
 import oracle
 import workloads
+from layer_wise_paged_gb300.batch import MappedHost
 from tests._host import GUARD, geom_of
+
+
+def mapped_copy(a: np.ndarray):
+    m = MappedHost(a.nbytes)
+    m.np[:a.nbytes] = a.view(np.uint8).reshape(-1)
+    return m
 
 
 def to_dev(a: np.ndarray | None):

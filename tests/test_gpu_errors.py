@@ -154,9 +154,11 @@ def test_host_side_checks_return_without_launching():
     assert kvl.kvl_batch_plan(g, gb.n_req, reqs, tabs, 1, plan, gb.plan_bytes - 1, s) == kvl.KVL_EINVAL
     bad = kvl.geom(SPEC.L, SPEC.P, SPEC.B, 24, SPEC.n_pool)
     assert kvl.kvl_merge_scatter_paged(bad, plan, reqs, tabs, 0, 1, pool, None, None, s) == kvl.KVL_EALIGN
-    # launch options: a negative CTA cap or a non-zero reserved field
+    # launch options: a negative CTA cap, an unknown flag, both host flags
     assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, -1, s) == kvl.KVL_EINVAL
-    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(4, 1),
+    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(4, 8),
+                                       s) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 3),
                                        s) == kvl.KVL_EINVAL
     # a plan built for another pool size is refused on the device
     other = kvl.geom(SPEC.L, SPEC.P, SPEC.B, SPEC.Rp, SPEC.n_pool - 1)

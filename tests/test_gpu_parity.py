@@ -17,7 +17,7 @@ import torch
 
 import oracle
 import workloads
-from tests._device import device_batch, one_layer_problem, sentinel_dev
+from tests._device import MappedHost, device_batch, mapped_copy, one_layer_problem, sentinel_dev
 from tests._host import GUARD, geom_of, host_buffers
 
 pytestmark = pytest.mark.gpu
@@ -215,6 +215,76 @@ def test_an_sm_budget_changes_nothing_but_speed(max_ctas):
         gb.scatter_back(layer, d.pool, max_ctas=max_ctas)
         assert ob.scatter_back(layer, hb.pool) == 0
     assert_bytes_equal(d.pool, hb.pool, "pool after scatter-back")
+    assert gb.status() == (0, 0)
+
+
+HOST_SPEC = dict(L=2, P=2, B=16, Rp=512, t_hit=[900, 0, 77, 410], t_miss=[20, 133, 0, 5],
+                 source="permuted", seed=95)
+
+
+def _host_batch(spec, hb, *, hit_host=False, miss_host=False, objects_host=False):
+    """A GPU batch whose chosen buffers live in pinned, mapped host memory."""
+    from layer_wise_paged_gb300.batch import Batch
+    from tests._device import to_dev
+    hit = mapped_copy(hb.hit) if hit_host else to_dev(hb.hit)
+    miss = mapped_copy(hb.miss) if miss_host else to_dev(hb.miss)
+    objects = mapped_copy(hb.objects) if objects_host else to_dev(hb.objects)
+    tables, src_tables, pool = to_dev(hb.tables), to_dev(hb.src_tables), to_dev(hb.pool)
+    g = (spec.L, spec.P, spec.B, spec.Rp, spec.n_pool)
+    b = Batch(g, hb.layout.requests, hit, miss, objects, tables, src_tables)
+    return b, hit, miss, objects, pool
+
+
+def test_merge_scatter_and_slice_read_a_host_full_block():
+    """DualPath's host buffer -> HBM leg: hit and miss rows read from pinned Grace
+    memory, written to the HBM pool and hit_layer."""
+    import layer_wise_paged_gb300 as kvl
+    spec = workloads.custom_spec(**HOST_SPEC)
+    hb = host_buffers(spec)
+    gb, hit, miss, objects, pool = _host_batch(spec, hb, hit_host=True, miss_host=True)
+    ob = oracle_batch(spec, hb)
+    gb.plan()
+    hit_out = sentinel_dev(ob.total_hit() * spec.R)
+    for layer in range(spec.L):
+        gb.slice_layer(layer, hit_out, flags=kvl.KVL_LAUNCH_HOST_SRC)
+        gb.merge_scatter(layer, pool, flags=kvl.KVL_LAUNCH_HOST_SRC)
+        want_hit = ob.slice_layer(layer)[1]
+        assert ob.merge_scatter(layer, hb.pool)[0] == 0
+        assert_bytes_equal(hit_out[:want_hit.size], want_hit, "hit_out")
+        assert_bytes_equal(pool, hb.pool, "pool")
+    # all layers in one launch as well (the final H2D of the whole prompt KV)
+    pool.fill_(SENT)
+    gb.merge_scatter(0, pool, layer_count=spec.L, flags=kvl.KVL_LAUNCH_HOST_SRC)
+    assert_bytes_equal(pool, hb.pool, "pool, one launch")
+    assert gb.status() == (0, 0)
+
+
+def test_gather_writes_host_objects_and_scatter_back_reads_them():
+    """Objects ready for transfer land in pinned host memory, and are restored from it."""
+    import layer_wise_paged_gb300 as kvl
+    spec = workloads.custom_spec(**HOST_SPEC, objects="block")
+    hb = host_buffers(spec)
+    gb, hit, miss, objects, pool = _host_batch(spec, hb, objects_host=True)
+    ob = oracle_batch(spec, hb)
+    gb.plan()
+    complete = MappedHost(ob.total_tokens() * spec.R + GUARD)
+    complete.np[:] = SENT
+    for layer in range(spec.L):
+        gb.merge_scatter(layer, pool, complete, flags=kvl.KVL_LAUNCH_HOST_DST)
+        gb.gather(layer, pool, flags=kvl.KVL_LAUNCH_HOST_DST)
+        torch.cuda.synchronize()
+        want_comp = ob.merge_scatter(layer, hb.pool, want_complete=True)[1]
+        assert ob.gather_objects(layer, hb.pool) == 0
+        assert np.array_equal(complete.np[:want_comp.size], want_comp)
+        assert np.all(complete.np[want_comp.size:] == SENT)
+        assert_bytes_equal(pool, hb.pool, "pool")
+        assert np.array_equal(objects.np[:hb.objects.size], hb.objects)
+    pool.fill_(SENT)
+    hb.pool[:] = SENT
+    gb.scatter_back(0, pool, layer_count=spec.L, flags=kvl.KVL_LAUNCH_HOST_SRC)
+    for layer in range(spec.L):
+        assert ob.scatter_back(layer, hb.pool) == 0
+    assert_bytes_equal(pool, hb.pool, "pool after scatter-back from host")
     assert gb.status() == (0, 0)
 
 
