@@ -389,13 +389,14 @@ def run_gpu(args):
             ("scatter_back", lambda l, n: b.scatter_back(l, pool, s, layer_count=n)),
         )
         for op, fn in phases:
-            for gi, (l0, n) in enumerate(groups):
-                if events is not None:
-                    events[op][gi][0].record(s)
-                    fn(l0, n)
-                    events[op][gi][1].record(s)
-                else:
-                    fn(l0, n)
+            # one event pair per phase, around all of its launches: an event between two
+            # kernels would end the programmatic dependent launch between them
+            if events is not None:
+                events[op][0].record(s)
+            for l0, n in groups:
+                fn(l0, n)
+            if events is not None:
+                events[op][1].record(s)
 
     def step(events=None, s=None):
         run_step(batch, s or stream, events)
@@ -414,7 +415,7 @@ def run_gpu(args):
     ev = None
     graph = None
     if not args.eager and make_event() is not None:
-        ev = {op: [(make_event(), make_event()) for _ in groups] for op in OPS}
+        ev = {op: (make_event(), make_event()) for op in OPS}
         graph = capture_step_graph(dev, stream, lambda s_: run_step(batch, s_, ev))
         for _ in range(2):
             graph.replay()
@@ -425,11 +426,11 @@ def run_gpu(args):
         if graph is not None:
             graph.replay()
         else:
-            evs = {op: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                        for _ in groups] for op in OPS}
+            evs = {op: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for op in OPS}
             step(evs)
             for op in OPS:
-                eager_ev[op].extend(evs[op])
+                eager_ev[op].append(evs[op])
 
     clocks_path = ROOT / "gpurun_out" / "clocks.csv" if (ROOT / "gpurun_out").is_dir() else None
     barrier(dist, dev)
@@ -449,15 +450,15 @@ def run_gpu(args):
     code, detail = batch.status(stream)
     if code != 0:
         raise SystemExit(f"bench.py: status {code} detail {detail} after the timed steps")
-    # per-kernel durations: the graph's events hold the last timed step's launches;
-    # eager mode keeps every timed launch
-    ev_used = ev if graph is not None else eager_ev
+    # per-launch durations: each op's phase time over its launches; the graph's events
+    # hold the last timed step, eager mode keeps every timed step
+    ev_used = {op: [ev[op]] for op in OPS} if graph is not None else eager_ev
 
     sb = step_bytes(spec)
     value = world * sb * args.steps / elapsed / 1e9
     per_op = {}
     for op in OPS:
-        ts = [a.elapsed_time(b) / 1e3 for a, b in ev_used[op]]
+        ts = [a.elapsed_time(b) / 1e3 / len(groups) for a, b in ev_used[op]]
         avg = sum(ts) / len(ts)
         per_op[op] = {"us_per_launch": round(avg * 1e6, 2),
                       "gbs": round(op_bytes(spec)[op] * spec.L / len(groups) / avg / 1e9, 1),
@@ -571,8 +572,9 @@ def run_gpu(args):
                    us_per_layer=round(elapsed / args.steps / spec.L * 1e6, 2),
                    launch="CUDA graph of one step, replayed per step" if graph is not None
                    else "eager C-ABI calls from Python",
-                   kernel_timing="events around each launch of the last timed step"
-                   if graph is not None else "events around every timed launch",
+                   kernel_timing="CUDA events around each op's phase of launches (launch "
+                   "duration = phase time / launches), last timed step" if graph is not None
+                   else "CUDA events around each op's phase of launches, every timed step",
                    step_bytes=sb, kernels=kernels, launches_per_step=launches_per_step,
                    parallelism=f"{world} independent replica(s)", gpu=torch.cuda.get_device_name(dev))
         line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
