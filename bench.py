@@ -432,7 +432,7 @@ def run_gpu(args):
             for op in OPS:
                 eager_ev[op].append(evs[op])
 
-    clocks_path = ROOT / "gpurun_out" / "clocks.csv" if (ROOT / "gpurun_out").is_dir() else None
+    clocks_path = Path(args.clocks_csv) if args.clocks_csv else None
     barrier(dist, dev)
     torch.cuda.synchronize(dev)
     t0 = torch.cuda.Event(enable_timing=True)
@@ -787,6 +787,8 @@ def parse_args(argv=None):
     p.add_argument("--gemm", type=int, default=4096, help="GEMM size of the --overlap compute")
     p.add_argument("--host-leg", action="store_true",
                    help="measure the host-buffer legs over NVLink-C2C")
+    p.add_argument("--clocks-csv", default="",
+                   help="also write the nvidia-smi clock samples of the timed region here")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-e2e", action="store_true")
