@@ -379,22 +379,35 @@ def run_gpu(args):
         except TypeError:
             return None
 
+    # Within an op's phase, the launches for successive layers touch disjoint bytes
+    # (their layers' pool regions, hit_layer buffers and object slots), so each may
+    # overlap the one before it.  A launch without the flag waits for everything before
+    # it: the first launch of a phase (it reads what the previous phase wrote), a slice
+    # launch that reuses a hit_layer buffer of the ring, and every gather when all
+    # layers share one layer of objects.
+    overlap = 0 if args.serial_launches else kvl.KVL_LAUNCH_OVERLAP_PREVIOUS
+
+    def launch_flags(op, i, l0):
+        if i == 0 or (op == "slice" and l0 % ring == 0) or (op == "gather" and one_layer):
+            return 0
+        return overlap
+
     def run_step(b, s, events):
-        """One step of batch b on stream s (timing events around each kernel, or None)."""
+        """One step of batch b on stream s (timing events around each phase, or None)."""
         b.plan(stream=s)
         phases = (
-            ("slice", lambda l, n: b.slice_layer(l, hit_views[l], s, layer_count=n)),
-            ("merge_scatter", lambda l, n: b.merge_scatter(l, pool, None, s, layer_count=n)),
-            ("gather", lambda l, n: b.gather(l, pool, s, layer_count=n)),
-            ("scatter_back", lambda l, n: b.scatter_back(l, pool, s, layer_count=n)),
+            ("slice", lambda l, n, f: b.slice_layer(l, hit_views[l], s, layer_count=n, flags=f)),
+            ("merge_scatter", lambda l, n, f: b.merge_scatter(l, pool, None, s, layer_count=n, flags=f)),
+            ("gather", lambda l, n, f: b.gather(l, pool, s, layer_count=n, flags=f)),
+            ("scatter_back", lambda l, n, f: b.scatter_back(l, pool, s, layer_count=n, flags=f)),
         )
         for op, fn in phases:
             # one event pair per phase, around all of its launches: an event between two
             # kernels would end the programmatic dependent launch between them
             if events is not None:
                 events[op][0].record(s)
-            for l0, n in groups:
-                fn(l0, n)
+            for i, (l0, n) in enumerate(groups):
+                fn(l0, n, launch_flags(op, i, l0))
             if events is not None:
                 events[op][1].record(s)
 
@@ -575,6 +588,10 @@ def run_gpu(args):
                    kernel_timing="CUDA events around each op's phase of launches (launch "
                    "duration = phase time / launches), last timed step" if graph is not None
                    else "CUDA events around each op's phase of launches, every timed step",
+                   launch_overlap="none: every launch waits for the one before it"
+                   if args.serial_launches else
+                   "KVL_LAUNCH_OVERLAP_PREVIOUS on a phase's launches after its first: "
+                   "each may start on the SMs its predecessor has left",
                    step_bytes=sb, kernels=kernels, launches_per_step=launches_per_step,
                    parallelism=f"{world} independent replica(s)", gpu=torch.cuda.get_device_name(dev))
         line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -794,6 +811,9 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--eager", action="store_true",
                    help="launch every call from Python instead of replaying a CUDA graph")
+    p.add_argument("--serial-launches", action="store_true",
+                   help="no launch starts before the one before it has finished (no "
+                        "KVL_LAUNCH_OVERLAP_PREVIOUS)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     a = p.parse_args(argv)
     if a.warmup < 3:

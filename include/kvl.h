@@ -108,7 +108,8 @@ typedef struct kvl_launch {
                          i.e. the copy occupies at most k SMs and leaves the rest to
                          concurrent work (an I/O SM budget, as Tutti 阅读笔记 设计二
                          gives its I/O kernels a fixed SM partition) */
-    int32_t flags;    /* 0, KVL_LAUNCH_HOST_SRC or KVL_LAUNCH_HOST_DST (not both) */
+    int32_t flags;    /* 0, or KVL_LAUNCH_HOST_SRC or KVL_LAUNCH_HOST_DST (not both),
+                         optionally OR KVL_LAUNCH_OVERLAP_PREVIOUS */
 } kvl_launch;
 
 /* The copy's sources (resp. destinations) are pinned host memory mapped into the
@@ -119,6 +120,21 @@ typedef struct kvl_launch {
  * side keeps the bulk-copy path.  Without the flag every buffer must be device memory. */
 #define KVL_LAUNCH_HOST_SRC 1
 #define KVL_LAUNCH_HOST_DST 2
+
+/* The call may start copying before the kernel enqueued just before it on the stream
+ * has finished, on the SMs that kernel has already left; it still finishes only after
+ * that kernel has (so a later call without the flag sees both complete).  Meant for
+ * the layer-wise pipeline's consecutive launches of one op on successive layers
+ * (Tutti 阅读笔记, 伪代码 1: one I/O launch per layer; layers touch disjoint pool
+ * regions), so that one launch's ramp-up fills the previous launch's tail.
+ * The caller guarantees that the call touches no byte that the kernels it may overlap
+ * write, and writes no byte that they read: the kernel just before it and, when that
+ * call carried the flag too, the kernels that call may overlap in turn.  Reads of the
+ * same plan, requests and tables are fine.  A call for the same plan, layer and op as
+ * the kernel before it must not carry the flag (the two would share a work counter).
+ * A call that overlaps a failing one may still copy: the failure shows in the plan's
+ * status (kvl_read_status) once both have finished. */
+#define KVL_LAUNCH_OVERLAP_PREVIOUS 4
 
 /* One request (device memory: the calls take an array of these in device memory).
  * All strides are in bytes. */
@@ -148,8 +164,9 @@ size_t kvl_plan_bytes(const kvl_geom *geom, int32_t n_req);
 /* Plan layout, for callers that read the plan's arrays (byte offsets into the plan):
  * off[0] header, off[1] tok_off (int64[n_req+1]), off[2] hit_off (int64[n_req+1]),
  * off[3] blk_off (int64[n_req+1]), off[4] item_req (int32[pool_blocks]),
- * off[5] item_blk (int32[pool_blocks]), off[6] item records, off[7] claim counters,
- * off[8] injectivity bitmap, off[9] total bytes.  The header's first int32 is the
+ * off[5] item_blk (int32[pool_blocks]), off[6] item records (always at byte 256),
+ * off[7] claim counters, off[8] injectivity bitmap (the last section), off[9] total
+ * bytes.  Sections are not placed in index order.  The header's first int32 is the
  * status and its int64 at byte 16 the item count. */
 void kvl_plan_layout(const kvl_geom *geom, int32_t n_req, size_t off[10]);
 
@@ -213,8 +230,13 @@ kvl_status kvl_batch_plan_static_scratch(const kvl_geom *geom, int32_t n_req,
  * layers ready, e.g. restoring a whole prefix (Tutti 阅读笔记, 伪代码 1 and its note:
  * the I/O kernel is loaded once per layer, O(L) launches, not O(L x blocks)).
  * layer >= 0, layer_count >= 1, layer + layer_count <= L, pool_blocks * layer_count
- * < 2^31; otherwise KVL_EINVAL.  `launch` may be NULL (the whole GPU); a negative
- * max_ctas, an unknown flag or both host flags together is KVL_EINVAL. */
+ * < 2^31; otherwise KVL_EINVAL.  `launch` may be NULL (the whole GPU, no flags); a
+ * negative max_ctas, an unknown flag or both host flags together is KVL_EINVAL.
+ * d_plan is a plan built for this geom: a device buffer of at least
+ * kvl_plan_layout(geom, 0)[8] bytes (true of any plan kvl_batch_plan accepted for it).
+ * The kernels read its item records before they check the header, so a buffer
+ * sized for a smaller pool may be read past its end; a plan built for other arrays or
+ * another geometry that is large enough is refused (KVL_EINVAL in its status). */
 
 /* kvl_slice_layer -- hit_layer[l] = hit_full_block[:, l] for every request
  * (DualPath KV Loading, "Dual-Path Loading": objects table and the slice_layer step

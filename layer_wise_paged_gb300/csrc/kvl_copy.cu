@@ -66,7 +66,7 @@ struct CopyArgs {
     uint8_t *out;  // hit_out (slice), complete_out (merge, may be null)
     int32_t P, B, Rp, layer, L;
     int32_t layer_count;  // layers [layer, layer + layer_count) in this launch
-    int32_t flags;        // KVL_LAUNCH_HOST_SRC / KVL_LAUNCH_HOST_DST
+    int32_t flags;        // KVL_LAUNCH_* of the call
     int64_t N;
 };
 
@@ -197,6 +197,23 @@ __device__ __forceinline__ void grid_dependency_wait()
 #if KVL_PDL
     asm volatile("griddepcontrol.wait;" ::: "memory");
 #endif
+}
+
+// Warm L2 with the line holding p.  A hint only: L2 is the device's point of
+// coherence, so a line fetched before a preceding kernel's writes land is updated by
+// them, and no later load can see it stale.
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// 32-bit load through the read-only path; volatile so that it is issued where it
+// stands, ahead of the loads that follow it.
+__device__ __forceinline__ uint32_t ld_nc_u32(const void *p)
+{
+    uint32_t r;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
@@ -391,10 +408,36 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
     __shared__ StageInfo info[kStages];
 
     const int lane = threadIdx.x;
-    // Everything this kernel reads may come from the previous kernel on the stream.
-    grid_dependency_wait();
+    const uint32_t smem0 = smem_u32(smem);
+    const uint32_t bar0 = smem_u32(bars);
+    if (lane == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+        fence_mbar_init();
+    }
+    // The item records sit at a fixed offset, so this CTA's first record (item
+    // blockIdx.x, below the plan's capacity of N records) is addressed without the
+    // header.  Its line and the header's are fetched into L2 while the previous kernel
+    // drains, and read together once it has finished.
+    const uint8_t *plan_bytes = static_cast<const uint8_t *>(a.plan);
+    const bool first_in_cap = blockIdx.x < a.N;
+    const uint32_t *first_rec = reinterpret_cast<const uint32_t *>(
+        plan_bytes + kRecordsOffset + int64_t(blockIdx.x) * int64_t(sizeof(ItemRec)));
+    if (lane == 0) prefetch_l2(plan_bytes);
+    if (lane == 1 && first_in_cap) prefetch_l2(first_rec);
+    __syncwarp();
+    // Everything this kernel reads may come from the previous kernel on the stream,
+    // unless the caller declared the two independent: then the wait moves to the end,
+    // so this kernel still completes after the previous one.
+    const bool overlap = (a.flags & KVL_LAUNCH_OVERLAP_PREVIOUS) != 0;
+    if (!overlap) grid_dependency_wait();
     allow_dependents_launch();
-    if (!plan_usable<OP>(a)) return;
+    const uint32_t rec_first = first_in_cap ? ld_nc_u32(first_rec + lane) : 0u;
+    if (!plan_usable<OP>(a)) {
+        if (lane == 0)
+            for (int s = 0; s < kStages; ++s) mbar_inval(bar0 + 8 * s);
+        if (overlap) grid_dependency_wait();
+        return;
+    }
     PlanHeader *h = static_cast<PlanHeader *>(a.plan);
     const PlanView v = plan_view(a.plan, h->n_req, h->pool_blocks, h->n_layers);
     const int64_t n_items = h->n_items;
@@ -405,14 +448,6 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
     const int row_bytes = OP == OP_SLICE ? a.P * a.Rp : a.Rp;
     const int max_rows = kStageBytes / row_bytes;  // >= 1 (host-checked)
     const int64_t R = int64_t(a.P) * a.Rp;
-
-    const uint32_t smem0 = smem_u32(smem);
-    const uint32_t bar0 = smem_u32(bars);
-    if (lane == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
 
     int64_t issued = 0, retired = 0;
     bool timed_out = false;
@@ -476,7 +511,8 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
     const int64_t n_hit_all = h->n_hit, n_tok_all = h->n_tokens;
     int64_t cur = blockIdx.x;
     const int64_t nxt_static = blockIdx.x + G;
-    uint32_t rec_cur = cur < n_units ? load_rec(item_of(cur)) : 0u;
+    // unit cur < n_items is item cur of the first layer: the record read above
+    uint32_t rec_cur = cur < n_items ? rec_first : cur < n_units ? load_rec(item_of(cur)) : 0u;
     uint32_t claim = 0;
     if (lane == 0) claim = atomicAdd(&ctr->next, 1u);
     for (bool first = true;; first = false) {
@@ -573,6 +609,7 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
             atomicExch(&ctr->done, 0u);
         }
     }
+    if (overlap) grid_dependency_wait();
 }
 
 // Diagnostic: the copy kernels' bounded wait, made to run out.  The barrier expects
@@ -678,8 +715,9 @@ kvl_status launch(const CopyArgs &args, const kvl_launch *opts, void *stream)
 {
     CopyArgs a = args;
     a.flags = opts ? opts->flags : 0;
-    if (a.flags == KVL_LAUNCH_HOST_SRC) return launch_mode<OP, 1>(a, opts, stream);
-    if (a.flags == KVL_LAUNCH_HOST_DST) return launch_mode<OP, 2>(a, opts, stream);
+    const int32_t host = a.flags & (KVL_LAUNCH_HOST_SRC | KVL_LAUNCH_HOST_DST);
+    if (host == KVL_LAUNCH_HOST_SRC) return launch_mode<OP, 1>(a, opts, stream);
+    if (host == KVL_LAUNCH_HOST_DST) return launch_mode<OP, 2>(a, opts, stream);
     return launch_mode<OP, 0>(a, opts, stream);
 }
 
@@ -689,8 +727,9 @@ kvl_status common_checks(const kvl_geom *g, const void *d_plan, const kvl_reques
 {
     const kvl_status s = check_geom(g);
     if (s) return s;
-    if (opts && (opts->max_ctas < 0 || (opts->flags & ~(KVL_LAUNCH_HOST_SRC | KVL_LAUNCH_HOST_DST)) ||
-                 opts->flags == (KVL_LAUNCH_HOST_SRC | KVL_LAUNCH_HOST_DST)))
+    constexpr int32_t kHostBoth = KVL_LAUNCH_HOST_SRC | KVL_LAUNCH_HOST_DST;
+    if (opts && (opts->max_ctas < 0 || (opts->flags & ~(kHostBoth | KVL_LAUNCH_OVERLAP_PREVIOUS)) ||
+                 (opts->flags & kHostBoth) == kHostBoth))
         return KVL_EINVAL;
     if (!d_plan || !d_reqs) return KVL_EINVAL;
     if (!aligned16(d_plan) || !aligned16(d_reqs)) return KVL_EALIGN;

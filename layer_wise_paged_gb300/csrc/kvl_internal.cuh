@@ -64,6 +64,8 @@ struct ClaimCounter {
     uint32_t done;
 };
 
+constexpr size_t kRecordsOffset = 256;  // the item records start right after the header
+
 // Byte offsets of the plan's sections (see kvl_plan_layout).
 struct PlanLayout {
     size_t off[10];
@@ -76,16 +78,19 @@ __host__ __device__ inline PlanLayout plan_layout(int32_t n_req, int64_t pool_bl
     size_t n1 = size_t(n_req < 0 ? 0 : n_req) + 1;
     size_t cap = size_t(pool_blocks < 0 ? 0 : pool_blocks);
     size_t L = size_t(n_layers < 0 ? 0 : n_layers);
+    // Placement: the item records come first, at a fixed offset, so a copy kernel can
+    // address its first record before it has read the header; the sections that
+    // depend on n_req follow; the bitmap is last.
     p.off[0] = 0;
-    p.off[1] = 256;
-    p.off[2] = p.off[1] + round256(n1 * 8);
-    p.off[3] = p.off[2] + round256(n1 * 8);
-    p.off[4] = p.off[3] + round256(n1 * 8);
-    p.off[5] = p.off[4] + round256(cap * 4);
-    p.off[6] = p.off[5] + round256(cap * 4);
-    p.off[7] = p.off[6] + round256(cap * sizeof(ItemRec));
-    p.off[8] = p.off[7] + round256(L * kOps * sizeof(ClaimCounter));
-    p.off[9] = p.off[8] + round256(((cap + 31) / 32) * 4);
+    p.off[6] = kRecordsOffset;                                        // item records
+    p.off[4] = p.off[6] + round256(cap * sizeof(ItemRec));           // item_req
+    p.off[5] = p.off[4] + round256(cap * 4);                         // item_blk
+    p.off[7] = p.off[5] + round256(cap * 4);                         // claim counters
+    p.off[1] = p.off[7] + round256(L * kOps * sizeof(ClaimCounter)); // tok_off
+    p.off[2] = p.off[1] + round256(n1 * 8);                          // hit_off
+    p.off[3] = p.off[2] + round256(n1 * 8);                          // blk_off
+    p.off[8] = p.off[3] + round256(n1 * 8);                          // bitmap
+    p.off[9] = p.off[8] + round256(((cap + 31) / 32) * 4);           // end
     return p;
 }
 

@@ -70,13 +70,16 @@ def test_plan_layout_is_consistent(lib):
     for L, n, N in [(1, 0, 1), (2, 1, 32), (61, 16, 10625), (32, 256, 49262), (80, 1000, 1 << 20)]:
         g = kvl.geom(L, 2, 16, 256, N)
         off = kvl.kvl_plan_layout(g, n)
-        assert off[0] == 0 and off[1] == 256
+        assert off[0] == 0 and off[6] == 256  # records right after the 256-byte header
         assert all(o % 256 == 0 for o in off)
-        assert off[2] - off[1] >= 8 * (n + 1) and off[4] - off[3] >= 8 * (n + 1)
-        assert off[5] - off[4] >= 4 * N and off[6] - off[5] >= 4 * N
-        assert off[7] - off[6] >= 128 * N          # item records
-        assert off[8] - off[7] >= 8 * 4 * L        # claim counters
-        assert off[9] - off[8] >= 4 * ((N + 31) // 32)
+        need = {1: 8 * (n + 1), 2: 8 * (n + 1), 3: 8 * (n + 1), 4: 4 * N, 5: 4 * N,
+                6: 128 * N, 7: 8 * 4 * L, 8: 4 * ((N + 31) // 32)}
+        starts = sorted((off[k], k) for k in need)
+        ends = [s for s, _ in starts[1:]] + [off[9]]
+        assert starts[0][0] >= 256
+        for (start, k), end in zip(starts, ends):
+            assert end - start >= need[k], k   # each section fits before the next one
+        assert starts[-1][1] == 8              # the bitmap is the last section
         assert kvl.kvl_plan_bytes(g, n) == off[9]
     assert kvl.kvl_plan_bytes(kvl.geom(0, 2, 16, 256, 8), 1) == 0
 

@@ -160,6 +160,10 @@ def test_host_side_checks_return_without_launching():
                                        s) == kvl.KVL_EINVAL
     assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 3),
                                        s) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 7),
+                                       s) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 12),
+                                       s) == kvl.KVL_EINVAL
     # a plan built for another pool size is refused on the device
     other = kvl.geom(SPEC.L, SPEC.P, SPEC.B, SPEC.Rp, SPEC.n_pool - 1)
     assert kvl.kvl_merge_scatter_paged(other, plan, reqs, tabs, 0, 1, pool, None, None, s) == kvl.KVL_OK

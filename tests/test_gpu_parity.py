@@ -218,6 +218,55 @@ def test_an_sm_budget_changes_nothing_but_speed(max_ctas):
     assert gb.status() == (0, 0)
 
 
+@pytest.mark.parametrize("budgets", [(None,), (5, None, 2, 11)])
+def test_overlapped_layer_launches_equal_the_oracle(budgets):
+    """Each op's launches for successive layers carry KVL_LAUNCH_OVERLAP_PREVIOUS (all
+    but the first of each phase): a launch may start while the one before it runs,
+    and a phase's first launch, which reads the previous phase's output, must still
+    see every earlier launch complete.  Mixed SM budgets let several launches of a
+    chain run at once."""
+    import layer_wise_paged_gb300 as kvl
+    ov = kvl.KVL_LAUNCH_OVERLAP_PREVIOUS
+    spec = workloads.custom_spec(L=8, P=2, B=16, Rp=1024, t_hit=[3000, 0, 777, 1410],
+                                 t_miss=[200, 1333, 0, 55], source="permuted", seed=97)
+    hb = host_buffers(spec)
+    gb, d = device_batch(spec, hb)
+    ob = oracle_batch(spec, hb)
+    gb.plan()
+    R = spec.R
+    n_hit, n_tok = ob.total_hit() * R, ob.total_tokens() * R
+    hit_out = sentinel_dev(spec.L * n_hit)
+    complete = sentinel_dev(spec.L * n_tok)
+
+    def opts(layer):
+        return dict(max_ctas=budgets[layer % len(budgets)], flags=ov if layer else 0)
+
+    for layer in range(spec.L):
+        gb.slice_layer(layer, hit_out[layer * n_hit:], **opts(layer))
+    for layer in range(spec.L):
+        gb.merge_scatter(layer, d.pool, complete[layer * n_tok:], **opts(layer))
+    for layer in range(spec.L):
+        gb.gather(layer, d.pool, **opts(layer))
+    want_hit = np.full(spec.L * n_hit + GUARD, SENT, np.uint8)
+    want_comp = np.full(spec.L * n_tok + GUARD, SENT, np.uint8)
+    for layer in range(spec.L):
+        want_hit[layer * n_hit:(layer + 1) * n_hit] = ob.slice_layer(layer)[1]
+        want_comp[layer * n_tok:(layer + 1) * n_tok] = ob.merge_scatter(
+            layer, hb.pool, want_complete=True)[1]
+        assert ob.gather_objects(layer, hb.pool) == 0
+    assert_bytes_equal(hit_out, want_hit, "hit_out")
+    assert_bytes_equal(complete, want_comp, "complete_out")
+    assert_bytes_equal(d.pool, hb.pool, "pool")
+    assert_bytes_equal(d.objects, hb.objects, "objects")
+    d.pool.fill_(SENT)
+    hb.pool[:] = SENT
+    for layer in range(spec.L):
+        gb.scatter_back(layer, d.pool, **opts(layer))
+        assert ob.scatter_back(layer, hb.pool) == 0
+    assert_bytes_equal(d.pool, hb.pool, "pool after scatter-back")
+    assert gb.status() == (0, 0)
+
+
 HOST_SPEC = dict(L=2, P=2, B=16, Rp=512, t_hit=[900, 0, 77, 410], t_miss=[20, 133, 0, 5],
                  source="permuted", seed=95)
 
