@@ -384,13 +384,17 @@ def run_gpu(args):
     # overlap the one before it.  A launch without the flag waits for everything before
     # it: the first launch of a phase (it reads what the previous phase wrote), a slice
     # launch that reuses a hit_layer buffer of the ring, and every gather when all
-    # layers share one layer of objects.
-    overlap = 0 if args.serial_launches else kvl.KVL_LAUNCH_OVERLAP_PREVIOUS
-
+    # layers share one layer of objects.  With shared objects the scatter-back launches
+    # do not overlap either: two of them running side by side would read the same
+    # object bytes at the same time, and the second would find them in L2.  A launch
+    # followed by overlapping ones leaves half of each SM's shared memory to them
+    # (KVL_LAUNCH_SHARE_SMS).
     def launch_flags(op, i, l0):
-        if i == 0 or (op == "slice" and l0 % ring == 0) or (op == "gather" and one_layer):
+        if args.serial_launches or (one_layer and op in ("gather", "scatter_back")):
             return 0
-        return overlap
+        if i == 0 or (op == "slice" and l0 % ring == 0):
+            return kvl.KVL_LAUNCH_SHARE_SMS if len(groups) > 1 else 0
+        return kvl.KVL_LAUNCH_OVERLAP_PREVIOUS
 
     def run_step(b, s, events):
         """One step of batch b on stream s (timing events around each phase, or None)."""
@@ -590,8 +594,13 @@ def run_gpu(args):
                    else "CUDA events around each op's phase of launches, every timed step",
                    launch_overlap="none: every launch waits for the one before it"
                    if args.serial_launches else
-                   "KVL_LAUNCH_OVERLAP_PREVIOUS on a phase's launches after its first: "
-                   "each may start on the SMs its predecessor has left",
+                   "as below, except gather and scatter-back (shared object layer), "
+                   "which run one launch at a time: KVL_LAUNCH_OVERLAP_PREVIOUS on a "
+                   "phase's launches after its first, KVL_LAUNCH_SHARE_SMS on the first"
+                   if one_layer else
+                   "KVL_LAUNCH_OVERLAP_PREVIOUS on a phase's launches after its first "
+                   "(each may start beside its predecessor, on half of an SM's shared "
+                   "memory), KVL_LAUNCH_SHARE_SMS on the first",
                    step_bytes=sb, kernels=kernels, launches_per_step=launches_per_step,
                    parallelism=f"{world} independent replica(s)", gpu=torch.cuda.get_device_name(dev))
         line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,

@@ -109,7 +109,8 @@ typedef struct kvl_launch {
                          concurrent work (an I/O SM budget, as Tutti 阅读笔记 设计二
                          gives its I/O kernels a fixed SM partition) */
     int32_t flags;    /* 0, or KVL_LAUNCH_HOST_SRC or KVL_LAUNCH_HOST_DST (not both),
-                         optionally OR KVL_LAUNCH_OVERLAP_PREVIOUS */
+                         optionally OR KVL_LAUNCH_OVERLAP_PREVIOUS and / or
+                         KVL_LAUNCH_SHARE_SMS */
 } kvl_launch;
 
 /* The copy's sources (resp. destinations) are pinned host memory mapped into the
@@ -135,6 +136,13 @@ typedef struct kvl_launch {
  * A call that overlaps a failing one may still copy: the failure shows in the plan's
  * status (kvl_read_status) once both have finished. */
 #define KVL_LAUNCH_OVERLAP_PREVIOUS 4
+
+/* Performance hint: the call's CTAs take half of an SM's shared memory (a 96 KiB
+ * pipeline instead of 192 KiB), so that a CTA of the next launch, if that one carries
+ * KVL_LAUNCH_OVERLAP_PREVIOUS, can run beside it on the same SM.  Set it on the call
+ * just before a run of overlapping calls; KVL_LAUNCH_OVERLAP_PREVIOUS implies it.  A
+ * call that runs alone is faster without it.  The host-memory variants ignore it. */
+#define KVL_LAUNCH_SHARE_SMS 8
 
 /* One request (device memory: the calls take an array of these in device memory).
  * All strides are in bytes. */

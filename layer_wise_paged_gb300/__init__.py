@@ -35,7 +35,7 @@ class kvl_launch(ctypes.Structure):
     _fields_ = [("max_ctas", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
-KVL_LAUNCH_HOST_SRC, KVL_LAUNCH_HOST_DST, KVL_LAUNCH_OVERLAP_PREVIOUS = 1, 2, 4
+KVL_LAUNCH_HOST_SRC, KVL_LAUNCH_HOST_DST, KVL_LAUNCH_OVERLAP_PREVIOUS, KVL_LAUNCH_SHARE_SMS = 1, 2, 4, 8
 
 
 class kvl_geom(ctypes.Structure):

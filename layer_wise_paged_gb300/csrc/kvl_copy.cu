@@ -25,7 +25,7 @@
 //     slots of one item and plane, at most one stage long, whose destination is
 //     contiguous), in bulk groups; a stage is refilled only after its store has read
 //     it (`cp.async.bulk.wait_group.read`).
-// Loads run up to kStages - 1 segments ahead of stores across item boundaries, so
+// Loads run up to STAGES - 1 segments ahead of stores across item boundaries, so
 // each SM keeps well over 100 KiB in flight with no registers holding data.  Every
 // mbarrier wait is bounded by the global timer: past the limit the kernel records
 // KVL_ETIMEOUT, waits (bounded again) for its copies in flight and returns.
@@ -38,25 +38,23 @@ namespace {
 
 enum Op { OP_SLICE = 0, OP_MERGE = 1, OP_GATHER = 2, OP_SCATTER = 3 };
 
-#ifndef KVL_STAGES
-#define KVL_STAGES 6
-#endif
-#ifndef KVL_STAGE_BYTES
-#define KVL_STAGE_BYTES (32 * 1024)
-#endif
-#ifndef KVL_CTAS_PER_SM
-#define KVL_CTAS_PER_SM 1
-#endif
 #ifndef KVL_PDL
 #define KVL_PDL 1
 #endif
 
-constexpr int kStages = KVL_STAGES;
-constexpr int kStageBytes = KVL_STAGE_BYTES;
-constexpr int kCtasPerSm = KVL_CTAS_PER_SM;
-constexpr int kLookahead = kStages - 1;
+// Pipeline depth.  A launch that has its SMs to itself keeps kDeepStages stages (192
+// KiB): one CTA must keep enough bytes in flight to hold its SM's share of the HBM
+// bandwidth.  A launch that may overlap the one before it (KVL_LAUNCH_OVERLAP_PREVIOUS),
+// or that precedes one (KVL_LAUNCH_SHARE_SMS), keeps kShallowStages (96 KiB), so a CTA
+// of each of two consecutive launches fits on one SM: while one launch drains its last
+// items, the next one's CTAs already stream, and two CTAs per SM together keep as many
+// bytes in flight as one deep CTA.
+constexpr int kStageBytes = 32 * 1024;
+constexpr int kDeepStages = 6;
+constexpr int kShallowStages = 3;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per mbarrier wait
-static_assert(kStageBytes % 16 == 0 && kStages >= 2, "stage geometry");
+static_assert(kStageBytes % 16 == 0 && kShallowStages >= 2 && kDeepStages >= kShallowStages,
+              "stage geometry");
 
 struct CopyArgs {
     void *plan;
@@ -400,9 +398,11 @@ struct StageInfo {
 
 // HOST: 0 = every buffer in device memory (bulk copies both ways), 1 = sources in
 // pinned host memory (SM loads), 2 = destinations in pinned host memory (SM stores).
-template <int OP, int HOST>
+template <int OP, int HOST, int STAGES>
 __device__ __forceinline__ void copy_rows(const CopyArgs &a)
 {
+    constexpr int kStages = STAGES;
+    constexpr int kLookahead = kStages - 1;
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ __align__(8) uint64_t bars[kStages];
     __shared__ StageInfo info[kStages];
@@ -638,58 +638,63 @@ __global__ void __launch_bounds__(32) kvl_wait_timeout_kernel(int32_t *status,
     if (threadIdx.x == 0) mbar_inval(b);
 }
 
-// One kernel per op for device buffers, so launch lists and profiles name the op; the
-// host-memory variants are separate instantiations, so the device path carries none of
-// their code.
-__global__ void __launch_bounds__(32) kvl_slice_kernel(CopyArgs a) { copy_rows<OP_SLICE, 0>(a); }
-__global__ void __launch_bounds__(32) kvl_merge_scatter_kernel(CopyArgs a) { copy_rows<OP_MERGE, 0>(a); }
-__global__ void __launch_bounds__(32) kvl_gather_kernel(CopyArgs a) { copy_rows<OP_GATHER, 0>(a); }
-__global__ void __launch_bounds__(32) kvl_scatter_back_kernel(CopyArgs a) { copy_rows<OP_SCATTER, 0>(a); }
+// One kernel per op for device buffers, so launch lists and profiles name the op, in
+// the two pipeline depths; the host-memory variants are separate instantiations (deep
+// only: their SM loads or stores, not the stage count, set their pace), so the device
+// path carries none of their code.
+template <int STAGES>
+__global__ void __launch_bounds__(32) kvl_slice_kernel(CopyArgs a) { copy_rows<OP_SLICE, 0, STAGES>(a); }
+template <int STAGES>
+__global__ void __launch_bounds__(32) kvl_merge_scatter_kernel(CopyArgs a) { copy_rows<OP_MERGE, 0, STAGES>(a); }
+template <int STAGES>
+__global__ void __launch_bounds__(32) kvl_gather_kernel(CopyArgs a) { copy_rows<OP_GATHER, 0, STAGES>(a); }
+template <int STAGES>
+__global__ void __launch_bounds__(32) kvl_scatter_back_kernel(CopyArgs a) { copy_rows<OP_SCATTER, 0, STAGES>(a); }
 
 template <int OP, int HOST>
 __global__ void __launch_bounds__(32) kvl_host_copy_kernel(CopyArgs a)
 {
-    copy_rows<OP, HOST>(a);
+    copy_rows<OP, HOST, kDeepStages>(a);
 }
 
-template <int OP, int HOST>
+template <int OP, int HOST, int STAGES>
 constexpr void (*kernel_of())(CopyArgs)
 {
     if constexpr (HOST != 0) {
         return kvl_host_copy_kernel<OP, HOST>;
     } else {
-        return OP == OP_SLICE ? kvl_slice_kernel
-             : OP == OP_MERGE ? kvl_merge_scatter_kernel
-             : OP == OP_GATHER ? kvl_gather_kernel
-                               : kvl_scatter_back_kernel;
+        return OP == OP_SLICE ? kvl_slice_kernel<STAGES>
+             : OP == OP_MERGE ? kvl_merge_scatter_kernel<STAGES>
+             : OP == OP_GATHER ? kvl_gather_kernel<STAGES>
+                               : kvl_scatter_back_kernel<STAGES>;
     }
 }
 
-constexpr int kSmemBytes = kStages * kStageBytes;
-
-// Grid: kCtasPerSm CTAs on every SM; opts each kernel into its shared memory once
-// per device.
-template <int OP, int HOST>
+// Grid: one CTA on every SM (or the caller's cap); opts each kernel into its shared
+// memory once per device.
+template <int OP, int HOST, int STAGES>
 int grid_size(const kvl_launch *opts)
 {
     static bool ready[kMaxDevices] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
     if (!ready[dev]) {
-        if (cudaFuncSetAttribute(kernel_of<OP, HOST>(), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBytes) != cudaSuccess)
+        if (cudaFuncSetAttribute(kernel_of<OP, HOST, STAGES>(),
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 STAGES * kStageBytes) != cudaSuccess)
             return 0;
         ready[dev] = true;
     }
-    const int full = kCtasPerSm * sm_count();
+    const int full = sm_count();
     if (opts && opts->max_ctas > 0 && opts->max_ctas < full) return opts->max_ctas;
     return full;
 }
 
-template <int OP, int HOST>
+template <int OP, int HOST, int STAGES>
 kvl_status launch_mode(const CopyArgs &a, const kvl_launch *opts, void *stream)
 {
-    const int grid = grid_size<OP, HOST>(opts);
+    constexpr int kSmemBytes = STAGES * kStageBytes;
+    const int grid = grid_size<OP, HOST, STAGES>(opts);
     if (grid <= 0) return KVL_ECUDA;
 #if KVL_PDL
     cudaLaunchConfig_t cfg = {};
@@ -702,10 +707,10 @@ kvl_status launch_mode(const CopyArgs &a, const kvl_launch *opts, void *stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kernel_of<OP, HOST>(), a) != cudaSuccess) return KVL_ECUDA;
+    if (cudaLaunchKernelEx(&cfg, kernel_of<OP, HOST, STAGES>(), a) != cudaSuccess) return KVL_ECUDA;
     return KVL_OK;
 #else
-    kernel_of<OP, HOST>()<<<grid, 32, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(a);
+    kernel_of<OP, HOST, STAGES>()<<<grid, 32, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(a);
     return launch_status();
 #endif
 }
@@ -716,9 +721,11 @@ kvl_status launch(const CopyArgs &args, const kvl_launch *opts, void *stream)
     CopyArgs a = args;
     a.flags = opts ? opts->flags : 0;
     const int32_t host = a.flags & (KVL_LAUNCH_HOST_SRC | KVL_LAUNCH_HOST_DST);
-    if (host == KVL_LAUNCH_HOST_SRC) return launch_mode<OP, 1>(a, opts, stream);
-    if (host == KVL_LAUNCH_HOST_DST) return launch_mode<OP, 2>(a, opts, stream);
-    return launch_mode<OP, 0>(a, opts, stream);
+    if (host == KVL_LAUNCH_HOST_SRC) return launch_mode<OP, 1, kDeepStages>(a, opts, stream);
+    if (host == KVL_LAUNCH_HOST_DST) return launch_mode<OP, 2, kDeepStages>(a, opts, stream);
+    if (a.flags & (KVL_LAUNCH_OVERLAP_PREVIOUS | KVL_LAUNCH_SHARE_SMS))
+        return launch_mode<OP, 0, kShallowStages>(a, opts, stream);
+    return launch_mode<OP, 0, kDeepStages>(a, opts, stream);
 }
 
 kvl_status common_checks(const kvl_geom *g, const void *d_plan, const kvl_request *d_reqs,
@@ -728,7 +735,8 @@ kvl_status common_checks(const kvl_geom *g, const void *d_plan, const kvl_reques
     const kvl_status s = check_geom(g);
     if (s) return s;
     constexpr int32_t kHostBoth = KVL_LAUNCH_HOST_SRC | KVL_LAUNCH_HOST_DST;
-    if (opts && (opts->max_ctas < 0 || (opts->flags & ~(kHostBoth | KVL_LAUNCH_OVERLAP_PREVIOUS)) ||
+    constexpr int32_t kKnown = kHostBoth | KVL_LAUNCH_OVERLAP_PREVIOUS | KVL_LAUNCH_SHARE_SMS;
+    if (opts && (opts->max_ctas < 0 || (opts->flags & ~kKnown) ||
                  (opts->flags & kHostBoth) == kHostBoth))
         return KVL_EINVAL;
     if (!d_plan || !d_reqs) return KVL_EINVAL;

@@ -156,13 +156,15 @@ def test_host_side_checks_return_without_launching():
     assert kvl.kvl_merge_scatter_paged(bad, plan, reqs, tabs, 0, 1, pool, None, None, s) == kvl.KVL_EALIGN
     # launch options: a negative CTA cap, an unknown flag, both host flags
     assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, -1, s) == kvl.KVL_EINVAL
-    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(4, 8),
+    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(4, 32),
                                        s) == kvl.KVL_EINVAL
     assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 3),
                                        s) == kvl.KVL_EINVAL
     assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 7),
                                        s) == kvl.KVL_EINVAL
-    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 12),
+    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 16),
+                                       s) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 11),
                                        s) == kvl.KVL_EINVAL
     # a plan built for another pool size is refused on the device
     other = kvl.geom(SPEC.L, SPEC.P, SPEC.B, SPEC.Rp, SPEC.n_pool - 1)

@@ -239,7 +239,8 @@ def test_overlapped_layer_launches_equal_the_oracle(budgets):
     complete = sentinel_dev(spec.L * n_tok)
 
     def opts(layer):
-        return dict(max_ctas=budgets[layer % len(budgets)], flags=ov if layer else 0)
+        return dict(max_ctas=budgets[layer % len(budgets)],
+                    flags=ov if layer else kvl.KVL_LAUNCH_SHARE_SMS * (len(budgets) > 1))
 
     for layer in range(spec.L):
         gb.slice_layer(layer, hit_out[layer * n_hit:], **opts(layer))
@@ -334,6 +335,32 @@ def test_gather_writes_host_objects_and_scatter_back_reads_them():
     for layer in range(spec.L):
         assert ob.scatter_back(layer, hb.pool) == 0
     assert_bytes_equal(pool, hb.pool, "pool after scatter-back from host")
+    assert gb.status() == (0, 0)
+
+
+def test_host_legs_with_overlapped_launches():
+    """The host-memory variants honour KVL_LAUNCH_OVERLAP_PREVIOUS too: successive
+    layers read from a pinned host full block, each launch overlapping the one before."""
+    import layer_wise_paged_gb300 as kvl
+    spec = workloads.custom_spec(**dict(HOST_SPEC, L=4))
+    hb = host_buffers(spec)
+    gb, hit, miss, objects, pool = _host_batch(spec, hb, hit_host=True, miss_host=True)
+    ob = oracle_batch(spec, hb)
+    gb.plan()
+    n_hit = ob.total_hit() * spec.R
+    hit_out = sentinel_dev(spec.L * n_hit)
+    src = kvl.KVL_LAUNCH_HOST_SRC
+    for layer in range(spec.L):
+        gb.slice_layer(layer, hit_out[layer * n_hit:],
+                       flags=src | (kvl.KVL_LAUNCH_OVERLAP_PREVIOUS if layer else 0))
+    for layer in range(spec.L):
+        gb.merge_scatter(layer, pool, flags=src | (kvl.KVL_LAUNCH_OVERLAP_PREVIOUS if layer else 0))
+    want_hit = np.full(spec.L * n_hit + GUARD, SENT, np.uint8)
+    for layer in range(spec.L):
+        want_hit[layer * n_hit:(layer + 1) * n_hit] = ob.slice_layer(layer)[1]
+        assert ob.merge_scatter(layer, hb.pool)[0] == 0
+    assert_bytes_equal(hit_out, want_hit, "hit_out")
+    assert_bytes_equal(pool, hb.pool, "pool")
     assert gb.status() == (0, 0)
 
 
