@@ -483,8 +483,12 @@ def run_gpu(args):
     dom = max(OPS, key=lambda o: per_op[o]["total_s"])
     peak, peak_kind = hbm_peak()
     achieved = per_op[dom]["gbs"]
-    traffic = recorded_traffic(KERNEL_NAMES[dom], spec.name) if K == 1 else None
-    roofline = {"bound": "hbm", "kernel": KERNEL_NAMES[dom] + f" ({dom})",
+    # the pipeline depth most of the dominant op's launches ran with (the kernels are
+    # instantiated per depth: 3 stages when sharing SMs with a neighbour launch, else 6)
+    shares = launch_flags(dom, 1, groups[1][0]) if len(groups) > 1 else 0
+    kname = f"{KERNEL_NAMES[dom]}<{3 if shares else 6}>"
+    traffic = recorded_traffic(kname, spec.name) if K == 1 else None
+    roofline = {"bound": "hbm", "kernel": kname + f" ({dom})",
                 "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                 "algorithmic_bytes_per_launch": op_bytes(spec)[dom] * spec.L // len(groups),
@@ -815,7 +819,7 @@ def parse_args(argv=None):
                    help="measure the host-buffer legs over NVLink-C2C")
     p.add_argument("--clocks-csv", default="",
                    help="also write the nvidia-smi clock samples of the timed region here")
-    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--e2e-steps", type=int, default=30)
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--eager", action="store_true",
