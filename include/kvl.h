@@ -189,8 +189,10 @@ void kvl_plan_layout(const kvl_geom *geom, int32_t n_req, size_t off[10]);
  * full-block id of a hit block (in [0, hit_src_blocks)) and, if check_injective,
  * that no pool block id repeats.
  *   geom            host pointer
- *   d_reqs          device array of n_req requests (caller-owned, read only)
- *   d_block_tables  device int32 tables, packed in request order (read only)
+ *   d_reqs          device array of n_req requests (caller-owned, read only; may be
+ *                   NULL when n_req == 0)
+ *   d_block_tables  device int32 tables, packed in request order (read only; may be
+ *                   NULL when n_req == 0)
  *   d_plan          device buffer of plan_bytes >= kvl_plan_bytes(geom, n_req) bytes,
  *                   16-byte aligned, caller-owned; overwritten.  The plan resolves
  *                   every item's addresses and block ids when it is built: later
@@ -244,7 +246,9 @@ kvl_status kvl_batch_plan_static_scratch(const kvl_geom *geom, int32_t n_req,
  * kvl_plan_layout(geom, 0)[8] bytes (true of any plan kvl_batch_plan accepted for it).
  * The kernels read its item records before they check the header, so a buffer
  * sized for a smaller pool may be read past its end; a plan built for other arrays or
- * another geometry that is large enough is refused (KVL_EINVAL in its status). */
+ * another geometry that is large enough is refused (KVL_EINVAL in its status).
+ * d_reqs and d_block_tables are the arrays the plan was built from; NULL only if it was
+ * built from NULL (a batch of no requests); other NULLs are refused on the device. */
 
 /* kvl_slice_layer -- hit_layer[l] = hit_full_block[:, l] for every request
  * (DualPath KV Loading, "Dual-Path Loading": objects table and the slice_layer step

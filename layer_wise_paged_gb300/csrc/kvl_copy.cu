@@ -739,7 +739,9 @@ kvl_status common_checks(const kvl_geom *g, const void *d_plan, const kvl_reques
     if (opts && (opts->max_ctas < 0 || (opts->flags & ~kKnown) ||
                  (opts->flags & kHostBoth) == kHostBoth))
         return KVL_EINVAL;
-    if (!d_plan || !d_reqs) return KVL_EINVAL;
+    // d_reqs may be NULL (a plan of no requests); the device compares it with the
+    // plan's own record of the array it was built from
+    if (!d_plan) return KVL_EINVAL;
     if (!aligned16(d_plan) || !aligned16(d_reqs)) return KVL_EALIGN;
     if (layer < 0 || layer_count < 1 || layer >= g->n_layers || layer_count > g->n_layers - layer)
         return KVL_EINVAL;
@@ -797,7 +799,7 @@ extern "C" kvl_status kvl_merge_scatter_paged(const kvl_geom *geom, const void *
     kvl_status s = common_checks(geom, d_plan, d_reqs, layer, layer_count,
                                  geom ? geom->plane_row_bytes : 0, opts);
     if (s) return s;
-    if (!d_block_tables || !d_pool) return KVL_EINVAL;
+    if (!d_pool) return KVL_EINVAL;  // d_block_tables: as d_reqs
     if ((reinterpret_cast<uintptr_t>(d_block_tables) & 3u) || !aligned16(d_pool) ||
         (d_complete_out && !aligned16(d_complete_out)))
         return KVL_EALIGN;
@@ -815,7 +817,7 @@ extern "C" kvl_status kvl_gather_layer_objects(const kvl_geom *geom, const void 
     kvl_status s = common_checks(geom, d_plan, d_reqs, layer, layer_count,
                                  geom ? geom->plane_row_bytes : 0, opts);
     if (s) return s;
-    if (!d_block_tables || !d_pool) return KVL_EINVAL;
+    if (!d_pool) return KVL_EINVAL;  // d_block_tables: as d_reqs
     if (direction != KVL_GATHER && direction != KVL_SCATTER_BACK) return KVL_EINVAL;
     if ((reinterpret_cast<uintptr_t>(d_block_tables) & 3u) || !aligned16(d_pool)) return KVL_EALIGN;
     const CopyArgs a =

@@ -166,6 +166,11 @@ def test_host_side_checks_return_without_launching():
                                        s) == kvl.KVL_EINVAL
     assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 11),
                                        s) == kvl.KVL_EINVAL
+    # a NULL request array is for plans of no requests: this plan refuses it on the device
+    assert kvl.kvl_merge_scatter_paged(g, plan, 0, tabs, 0, 1, pool, None, None, s) == kvl.KVL_OK
+    assert gb.status()[0] == kvl.KVL_EINVAL
+    gb.plan()
+    assert gb.status() == (0, 0)
     # a plan built for another pool size is refused on the device
     other = kvl.geom(SPEC.L, SPEC.P, SPEC.B, SPEC.Rp, SPEC.n_pool - 1)
     assert kvl.kvl_merge_scatter_paged(other, plan, reqs, tabs, 0, 1, pool, None, None, s) == kvl.KVL_OK

@@ -143,6 +143,44 @@ def test_scaled_workload_shapes_bit_exact(name):
     run_parity(workloads.custom_spec(name, **SCALED[name], seed=31))
 
 
+EDGE = {
+    # degenerate batches: no requests at all, only empty requests, empty requests
+    # between others, a single token
+    "no_requests": dict(L=2, P=2, B=16, Rp=256, t_hit=[], t_miss=[]),
+    "only_empty_requests": dict(L=2, P=2, B=16, Rp=256, t_hit=[0, 0], t_miss=[0, 0]),
+    "empty_requests_between": dict(L=3, P=2, B=16, Rp=64, t_hit=[0, 17, 0, 0], t_miss=[0, 0, 5, 0]),
+    "one_token": dict(L=1, P=2, B=64, Rp=16, t_hit=[0], t_miss=[1]),
+    # the largest rows a 32 KiB stage holds: a 32 KiB slice row (2 planes of 16 KiB)
+    # and a 32 KiB plane row
+    "largest_slice_row": dict(L=2, P=2, B=2, Rp=16384, t_hit=[3, 0, 1], t_miss=[2, 1, 0]),
+    "largest_plane_row": dict(L=2, P=1, B=3, Rp=32768, t_hit=[4, 1], t_miss=[0, 3]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(EDGE))
+def test_edge_shapes_bit_exact(name):
+    run_parity(workloads.custom_spec(**EDGE[name], source="permuted", seed=301))
+
+
+def test_rows_larger_than_a_stage_are_refused():
+    """A slice row of two 32 KiB planes does not fit a 32 KiB stage: the slice is refused
+    on the host; the per-plane ops, whose rows are one plane, still run."""
+    import layer_wise_paged_gb300 as kvl
+    spec = workloads.custom_spec(L=1, P=2, B=2, Rp=32768, t_hit=[3], t_miss=[1], seed=302)
+    hb = host_buffers(spec)
+    gb, d = device_batch(spec, hb)
+    ob = oracle_batch(spec, hb)
+    gb.plan()
+    out = sentinel_dev(ob.total_hit() * spec.R)
+    s = torch.cuda.current_stream().cuda_stream
+    assert kvl.kvl_slice_layer(gb.g, gb.d_plan.data_ptr(), gb.d_reqs.data_ptr(), 0, 1,
+                               out.data_ptr(), None, s) == kvl.KVL_EINVAL
+    gb.merge_scatter(0, d.pool)
+    assert ob.merge_scatter(0, hb.pool)[0] == 0
+    assert_bytes_equal(d.pool, hb.pool, "pool")
+    assert gb.status() == (0, 0)
+
+
 def test_without_injectivity_check_results_are_unchanged():
     spec = workloads.custom_spec(L=2, P=2, B=16, Rp=256, t_hit=[300, 5], t_miss=[20, 40])
     run_parity(spec, check_injective=False)
