@@ -671,19 +671,19 @@ constexpr void (*kernel_of())(CopyArgs)
 }
 
 // Grid: one CTA on every SM (or the caller's cap); opts each kernel into its shared
-// memory once per device.
+// memory once per device (concurrent first calls may both set the same attribute).
 template <int OP, int HOST, int STAGES>
 int grid_size(const kvl_launch *opts)
 {
-    static bool ready[kMaxDevices] = {false};
+    static std::atomic<bool> ready[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
-    if (!ready[dev]) {
+    if (!ready[dev].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(kernel_of<OP, HOST, STAGES>(),
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  STAGES * kStageBytes) != cudaSuccess)
             return 0;
-        ready[dev] = true;
+        ready[dev].store(true, std::memory_order_release);
     }
     const int full = sm_count();
     if (opts && opts->max_ctas > 0 && opts->max_ctas < full) return opts->max_ctas;

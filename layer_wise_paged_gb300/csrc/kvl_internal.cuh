@@ -2,6 +2,7 @@
 // libkvl.so: the plan's device layout, status recording, and host-side checks.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -156,18 +157,20 @@ inline kvl_status check_geom(const kvl_geom *g)
 }
 
 // SM count of the current device (cached per device).
+// SMs of the current device, cached per device (host threads may call concurrently:
+// each may query the attribute once and store the same value).
 inline int sm_count()
 {
-    static int cache[kMaxDevices] = {0};
+    static std::atomic<int> cache[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (dev < 0 || dev >= kMaxDevices) return 0;
-    if (cache[dev] == 0) {
-        int n = 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
 }
 
 inline kvl_status launch_status()
