@@ -220,6 +220,22 @@ def recorded_traffic(kernel: str, workload: str):
 # CPU oracle on a bounded sample (baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
+def phase_launch_flags(op, i, l0, *, ring, n_launches, shared_objects, serial):
+    """Flags of launch i (first layer l0) of an op's phase of n_launches launches.
+
+    A launch may overlap the one before it only when the two touch disjoint bytes:
+    never the first launch of a phase (it reads the previous phase's output), never a
+    slice launch that reuses a buffer of the hit_layer ring (l0 a multiple of `ring`),
+    and no gather or scatter-back launch when all layers share one layer of objects.
+    The launch before a run of overlapping ones leaves them half of each SM."""
+    from layer_wise_paged_gb300 import KVL_LAUNCH_OVERLAP_PREVIOUS, KVL_LAUNCH_SHARE_SMS
+    if serial or (shared_objects and op in ("gather", "scatter_back")):
+        return 0
+    if i == 0 or (op == "slice" and l0 % ring == 0):
+        return KVL_LAUNCH_SHARE_SMS if n_launches > 1 else 0
+    return KVL_LAUNCH_OVERLAP_PREVIOUS
+
+
 def _layer_shifted(requests, layer):
     """Request layouts whose layer-0 view is `layer` of the original (pointer shift)."""
     return [dataclasses.replace(q, hit_off=q.hit_off + layer * q.hit_layer_stride,
@@ -309,7 +325,8 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-            "config": describe(spec),
+            "config": dict(describe(spec), us_per_layer=round(dt / args.steps * 1e6, 1),
+                           layers_per_s=round(args.steps / dt, 3)),
             "cpu_baseline": {"value": round(v, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": f"{spec.name}: one layer per step (all four ops), "
                                        "single-threaded C oracle"},
@@ -390,11 +407,8 @@ def run_gpu(args):
     # followed by overlapping ones leaves half of each SM's shared memory to them
     # (KVL_LAUNCH_SHARE_SMS).
     def launch_flags(op, i, l0):
-        if args.serial_launches or (one_layer and op in ("gather", "scatter_back")):
-            return 0
-        if i == 0 or (op == "slice" and l0 % ring == 0):
-            return kvl.KVL_LAUNCH_SHARE_SMS if len(groups) > 1 else 0
-        return kvl.KVL_LAUNCH_OVERLAP_PREVIOUS
+        return phase_launch_flags(op, i, l0, ring=ring, n_launches=len(groups),
+                                  shared_objects=one_layer, serial=args.serial_launches)
 
     def run_step(b, s, events):
         """One step of batch b on stream s (timing events around each phase, or None)."""
@@ -479,6 +493,7 @@ def run_gpu(args):
         avg = sum(ts) / len(ts)
         per_op[op] = {"us_per_launch": round(avg * 1e6, 2),
                       "gbs": round(op_bytes(spec)[op] * spec.L / len(groups) / avg / 1e9, 1),
+                      "layers_per_s": round(spec.L / len(groups) / avg, 1),
                       "total_s": sum(ts)}
     dom = max(OPS, key=lambda o: per_op[o]["total_s"])
     peak, peak_kind = hbm_peak()
@@ -591,6 +606,7 @@ def run_gpu(args):
                    objects="one layer (layer stride 0)" if one_layer else "all layers",
                    hit_layer_buffers=ring,
                    us_per_layer=round(elapsed / args.steps / spec.L * 1e6, 2),
+                   layers_per_s=round(world * spec.L * args.steps / elapsed, 1),
                    launch="CUDA graph of one step, replayed per step" if graph is not None
                    else "eager C-ABI calls from Python",
                    kernel_timing="CUDA events around each op's phase of launches (launch "

@@ -1,0 +1,101 @@
+"""Host logic of bench.py, on the CPU: the algorithmic byte counts behind every GB/s
+figure, the launch-flag rule that decides which launches may overlap, the traffic
+record lookup and the reference arm's JSON line."""
+from __future__ import annotations
+
+import contextlib
+import io
+import json
+
+import pytest
+
+import bench
+import layer_wise_paged_gb300 as kvl
+import workloads
+
+OV, SH = kvl.KVL_LAUNCH_OVERLAP_PREVIOUS, kvl.KVL_LAUNCH_SHARE_SMS
+
+
+def test_llama_layer_bytes_follow_the_kv_size_formula():
+    # KV bytes of one layer = 2 (K, V) * T * H_kv * d * 2 bytes (bf16); each op reads
+    # its bytes once and writes them once
+    spec = workloads.get_spec("llama3_8b_agentic")
+    T_hit, T_all = 30720, 30720 + 512
+    layer_kv = lambda T: 2 * T * 8 * 128 * 2
+    b = bench.op_bytes(spec)
+    assert b["slice"] == 2 * layer_kv(T_hit)
+    assert b["merge_scatter"] == 2 * layer_kv(T_all)
+    # objects carry whole blocks: ceil(T_all / 16) blocks of 16 slots per plane
+    nblk = -(-T_all // 16)
+    assert b["gather"] == b["scatter_back"] == 2 * 2 * nblk * 16 * 2048
+    assert bench.step_bytes(spec) == spec.L * sum(b.values())
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3_32b_long", "latent_batch", "many_small"])
+def test_op_bytes_match_the_spec(name):
+    spec = workloads.get_spec(name)
+    b = bench.op_bytes(spec)
+    t_hit, t_all = sum(spec.t_hit), sum(spec.t_hit) + sum(spec.t_miss)
+    assert b["slice"] == 2 * t_hit * spec.R
+    assert b["merge_scatter"] == 2 * t_all * spec.R
+    assert b["gather"] == 2 * spec.P * int(spec.nblk().sum()) * spec.B * spec.Rp
+
+
+def _flags(op, n, *, ring=8, shared=False, serial=False, K=1):
+    return [bench.phase_launch_flags(op, i, i * K, ring=ring, n_launches=n,
+                                     shared_objects=shared, serial=serial) for i in range(n)]
+
+
+def test_first_launch_of_a_phase_never_overlaps():
+    for op in bench.OPS:
+        f = _flags(op, 32)
+        assert f[0] == SH and not f[0] & OV
+        assert all(x == OV for x in f[1:]) or op == "slice"
+
+
+def test_slice_launches_that_reuse_a_ring_buffer_wait():
+    f = _flags("slice", 32, ring=8)
+    for i, x in enumerate(f):
+        assert (x & OV == 0) == (i % 8 == 0), i
+    # several layers per launch: ring is a multiple of K, the check is on first layers
+    f = _flags("slice", 8, ring=8, K=4)
+    assert [bool(x & OV) for x in f] == [False, True, False, True, False, True, False, True]
+
+
+def test_shared_object_layer_keeps_gather_and_scatter_back_alone():
+    assert _flags("gather", 32, shared=True) == [0] * 32
+    assert _flags("scatter_back", 32, shared=True) == [0] * 32
+    assert _flags("merge_scatter", 32, shared=True)[1:] == [OV] * 31
+
+
+def test_serial_and_single_launch_phases_carry_no_flags():
+    for op in bench.OPS:
+        assert _flags(op, 32, serial=True) == [0] * 32
+        assert _flags(op, 1) == [0]
+
+
+def test_traffic_record_is_read_only_for_the_current_kernel_source():
+    h = bench.kernel_source_hash()
+    rec = [line.split() for line in (bench.ROOT / "profiles" / "dram_traffic.txt").read_text()
+           .splitlines() if line and not line.startswith("#")]
+    for kernel, workload, sha, nbytes in rec:
+        got = bench.recorded_traffic(kernel, workload)
+        assert got == (int(nbytes) if sha == h else None)
+    assert bench.recorded_traffic("no_such_kernel", "llama3_8b_agentic") is None
+
+
+def test_reference_arm_prints_one_json_line():
+    out = io.StringIO()
+    with contextlib.redirect_stdout(out):
+        rc = bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "2",
+                         "--warmup", "3"])
+    assert rc == 0
+    lines = [x for x in out.getvalue().splitlines() if x.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == bench.UNIT and d["metric"] == bench.METRIC
+    assert d["value"] > 0 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": bench.UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"] == "tiny"
