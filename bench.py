@@ -340,6 +340,66 @@ def run_reference(args):
 # The GPU arm
 # ---------------------------------------------------------------------------
 
+class BenchStep:
+    """The buffers and launches of one bench step on a workload.
+
+    A step is the plan, then every layer's slice, merge-scatter, gather and
+    scatter-back, op by op (all layers of one op, then the next), K layers per launch.
+    hit_layer[l] goes to a ring of HIT_RING per-layer buffers: each is rewritten only
+    after several other layers' traffic has pushed its lines out of L2.  The largest
+    workloads keep one layer of objects (object layer stride 0, each layer's gather
+    lands in the same > L2-sized region) to fit in HBM."""
+
+    def __init__(self, spec, dev, layers_per_launch=1, serial=False):
+        import torch
+        from layer_wise_paged_gb300.batch import Batch
+        self.spec, self.serial = spec, serial
+        self.one_layer = workloads.footprint_bytes(spec) > 160e9
+        self.bufs = workloads.allocate(spec, dev, objects_one_layer=self.one_layer)
+        lay = self.bufs["layout"]
+        self.geom = (spec.L, spec.P, spec.B, spec.Rp, spec.n_pool)
+        self.batch = Batch(self.geom, lay.requests, self.bufs["hit"], self.bufs["miss"],
+                           self.bufs["objects"], self.bufs["tables"], self.bufs["src_tables"])
+        self.pool = self.bufs["pool"]
+        self.K = K = max(1, min(layers_per_launch, spec.L))
+        self.groups = [(l0, min(K, spec.L - l0)) for l0 in range(0, spec.L, K)]
+        self.ring = min(spec.L, -(-max(HIT_RING, K) // K) * K)
+        self.layer_hit = self.batch.total_hit * spec.R
+        self.hit_out = torch.empty(max(16, self.ring * self.layer_hit), dtype=torch.uint8,
+                                   device=dev)
+        self.hit_views = [self.hit_out[(l % self.ring) * self.layer_hit:] for l in range(spec.L)]
+
+    def flags(self, op, i, l0):
+        """Launch flags of launch i (first layer l0) of op's phase (phase_launch_flags)."""
+        return phase_launch_flags(op, i, l0, ring=self.ring, n_launches=len(self.groups),
+                                  shared_objects=self.one_layer, serial=self.serial)
+
+    def phases(self, b, s):
+        """(op, [launch thunks]) for each phase of batch b's step on stream s."""
+        pool, hv = self.pool, self.hit_views
+        calls = {
+            "slice": lambda l, n, f: b.slice_layer(l, hv[l], s, layer_count=n, flags=f),
+            "merge_scatter": lambda l, n, f: b.merge_scatter(l, pool, None, s, layer_count=n, flags=f),
+            "gather": lambda l, n, f: b.gather(l, pool, s, layer_count=n, flags=f),
+            "scatter_back": lambda l, n, f: b.scatter_back(l, pool, s, layer_count=n, flags=f),
+        }
+        return [(op, [(lambda fn=calls[op], l0=l0, n=n, f=self.flags(op, i, l0): fn(l0, n, f))
+                      for i, (l0, n) in enumerate(self.groups)]) for op in OPS]
+
+    def enqueue(self, b, s, events=None):
+        """One step of batch b on stream s; events[op] = (start, end) around each phase."""
+        b.plan(stream=s)
+        for op, launches in self.phases(b, s):
+            # one event pair per phase, around all of its launches: an event between two
+            # kernels would end the programmatic dependent launch between them
+            if events is not None:
+                events[op][0].record(s)
+            for launch in launches:
+                launch()
+            if events is not None:
+                events[op][1].record(s)
+
+
 def capture_step_graph(dev, stream, fn):
     """A CUDA graph of fn(stream): one eager run on a side stream first (outside capture,
     so the library's per-device caches are filled), then the capture."""
@@ -371,23 +431,11 @@ def run_gpu(args):
     kvl.lib()
 
     spec = bench_spec(args)
-    # The largest workloads keep one layer of objects (object layer stride 0, each
-    # layer's gather lands in the same > L2-sized region) to fit in HBM.
-    one_layer = workloads.footprint_bytes(spec) > 160e9
-    bufs = workloads.allocate(spec, dev, objects_one_layer=one_layer)
-    lay = bufs["layout"]
-    g = (spec.L, spec.P, spec.B, spec.Rp, spec.n_pool)
-    batch = Batch(g, lay.requests, bufs["hit"], bufs["miss"], bufs["objects"], bufs["tables"],
-                  bufs["src_tables"])
-    pool = bufs["pool"]
-    # hit_layer[l] goes to a ring of HIT_RING per-layer buffers: each is rewritten only
-    # after several other layers' traffic has pushed its lines out of L2
-    K = max(1, min(args.layers_per_launch, spec.L))  # layers per launch
-    groups = [(l0, min(K, spec.L - l0)) for l0 in range(0, spec.L, K)]
-    ring = min(spec.L, -(-max(HIT_RING, K) // K) * K)
-    layer_hit = batch.total_hit * spec.R
-    hit_out = torch.empty(max(16, ring * layer_hit), dtype=torch.uint8, device=dev)
-    hit_views = [hit_out[(l % ring) * layer_hit:] for l in range(spec.L)]
+    bs = BenchStep(spec, dev, layers_per_launch=args.layers_per_launch,
+                   serial=args.serial_launches)
+    bufs, lay, g, batch, pool = bs.bufs, bs.bufs["layout"], bs.geom, bs.batch, bs.pool
+    K, groups, ring, one_layer = bs.K, bs.groups, bs.ring, bs.one_layer
+    launch_flags = bs.flags
     stream = torch.cuda.current_stream(dev)
 
     def make_event():
@@ -396,38 +444,8 @@ def run_gpu(args):
         except TypeError:
             return None
 
-    # Within an op's phase, the launches for successive layers touch disjoint bytes
-    # (their layers' pool regions, hit_layer buffers and object slots), so each may
-    # overlap the one before it.  A launch without the flag waits for everything before
-    # it: the first launch of a phase (it reads what the previous phase wrote), a slice
-    # launch that reuses a hit_layer buffer of the ring, and every gather when all
-    # layers share one layer of objects.  With shared objects the scatter-back launches
-    # do not overlap either: two of them running side by side would read the same
-    # object bytes at the same time, and the second would find them in L2.  A launch
-    # followed by overlapping ones leaves half of each SM's shared memory to them
-    # (KVL_LAUNCH_SHARE_SMS).
-    def launch_flags(op, i, l0):
-        return phase_launch_flags(op, i, l0, ring=ring, n_launches=len(groups),
-                                  shared_objects=one_layer, serial=args.serial_launches)
-
     def run_step(b, s, events):
-        """One step of batch b on stream s (timing events around each phase, or None)."""
-        b.plan(stream=s)
-        phases = (
-            ("slice", lambda l, n, f: b.slice_layer(l, hit_views[l], s, layer_count=n, flags=f)),
-            ("merge_scatter", lambda l, n, f: b.merge_scatter(l, pool, None, s, layer_count=n, flags=f)),
-            ("gather", lambda l, n, f: b.gather(l, pool, s, layer_count=n, flags=f)),
-            ("scatter_back", lambda l, n, f: b.scatter_back(l, pool, s, layer_count=n, flags=f)),
-        )
-        for op, fn in phases:
-            # one event pair per phase, around all of its launches: an event between two
-            # kernels would end the programmatic dependent launch between them
-            if events is not None:
-                events[op][0].record(s)
-            for i, (l0, n) in enumerate(groups):
-                fn(l0, n, launch_flags(op, i, l0))
-            if events is not None:
-                events[op][1].record(s)
+        bs.enqueue(b, s, events)
 
     def step(events=None, s=None):
         run_step(batch, s or stream, events)
