@@ -22,6 +22,7 @@ import dataclasses
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -194,9 +195,16 @@ def hbm_peak():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the code the kernels are built from (the CUDA sources and the C ABI
+    header), comments and blank lines left out, so that a change of wording does not
+    make a recorded ncu measurement stale."""
     h = hashlib.sha256()
-    for f in sorted((ROOT / "layer_wise_paged_gb300" / "csrc").glob("*")):
-        h.update(f.read_bytes())
+    files = sorted((ROOT / "layer_wise_paged_gb300" / "csrc").glob("*")) + [ROOT / "include" / "kvl.h"]
+    for f in files:
+        text = re.sub(r"/\*.*?\*/", "", f.read_text(), flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code = "\n".join(line.strip() for line in text.splitlines() if line.strip())
+        h.update(f.name.encode() + b"\0" + code.encode() + b"\0")
     return h.hexdigest()[:16]
 
 

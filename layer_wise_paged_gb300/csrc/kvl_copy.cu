@@ -26,9 +26,16 @@
 //     contiguous), in bulk groups; a stage is refilled only after its store has read
 //     it (`cp.async.bulk.wait_group.read`).
 // Loads run up to STAGES - 1 segments ahead of stores across item boundaries, so
-// each SM keeps well over 100 KiB in flight with no registers holding data.  Every
-// mbarrier wait is bounded by the global timer: past the limit the kernel records
+// each SM keeps over 100 KiB in flight (one 6-stage CTA, or two 3-stage CTAs of
+// consecutive launches side by side) with no registers holding data.  Every mbarrier
+// wait is bounded by the global timer: past the limit the kernel records
 // KVL_ETIMEOUT, waits (bounded again) for its copies in flight and returns.
+//
+// Ordering between launches: programmatic dependent launch.  A kernel lets its
+// successor launch as soon as it starts, and waits for its predecessor
+// (griddepcontrol.wait) before its first read, or, when the caller declared the two
+// independent (KVL_LAUNCH_OVERLAP_PREVIOUS), just before it exits, so it still
+// completes after its predecessor.
 #include <cstdint>
 
 #include "kvl_internal.cuh"
