@@ -376,6 +376,71 @@ def test_gather_writes_host_objects_and_scatter_back_reads_them():
     assert gb.status() == (0, 0)
 
 
+@pytest.mark.parametrize("case", range(10))
+def test_random_launch_plans_equal_the_oracle(case):
+    """Random ragged batches under random launch plans: per op, random layers per
+    launch, SM budgets and overlap flags (every launch of a phase after the first may
+    overlap its predecessor; the first shares SMs or not).  Budgets as small as one
+    CTA let long chains of launches run at once."""
+    import layer_wise_paged_gb300 as kvl
+    g = np.random.default_rng(7100 + case)
+    L = int(g.integers(2, 7))
+    n = int(g.choice([1, 3, 9]))
+    spec = workloads.custom_spec(
+        L=L, P=int(g.integers(1, 3)), B=int(g.choice([4, 16, 64])),
+        Rp=int(g.choice([64, 1152, 2048])), t_hit=g.integers(0, 900, n),
+        t_miss=g.integers(0, 300, n), table=str(g.choice(["perm", "fragmented"])),
+        source=str(g.choice(["contiguous", "permuted"])), seed=7200 + case,
+        objects=str(g.choice(["layer", "block"])))
+    hb = host_buffers(spec)
+    gb, d = device_batch(spec, hb)
+    ob = oracle_batch(spec, hb)
+    gb.plan()
+    R = spec.R
+    n_hit, n_tok = ob.total_hit() * R, ob.total_tokens() * R
+    hit_out = sentinel_dev(L * n_hit)
+    complete = sentinel_dev(L * n_tok)
+
+    def plan_of_launches():
+        K = int(g.integers(1, L + 1))
+        out = []
+        for i, l0 in enumerate(range(0, L, K)):
+            f = 0
+            if i == 0 and g.random() < 0.5:
+                f = kvl.KVL_LAUNCH_SHARE_SMS
+            elif i > 0 and g.random() < 0.8:
+                f = kvl.KVL_LAUNCH_OVERLAP_PREVIOUS
+            out.append((l0, min(K, L - l0), dict(max_ctas=[None, 1, 5, 40][int(g.integers(0, 4))],
+                                                  flags=f)))
+        return out
+
+    for l0, k, o in plan_of_launches():
+        gb.slice_layer(l0, hit_out[l0 * n_hit:], layer_count=k, **o)
+    for l0, k, o in plan_of_launches():
+        gb.merge_scatter(l0, d.pool, complete[l0 * n_tok:], layer_count=k, **o)
+    for l0, k, o in plan_of_launches():
+        gb.gather(l0, d.pool, layer_count=k, **o)
+    want_hit = np.full(L * n_hit + GUARD, SENT, np.uint8)
+    want_comp = np.full(L * n_tok + GUARD, SENT, np.uint8)
+    for layer in range(L):
+        want_hit[layer * n_hit:(layer + 1) * n_hit] = ob.slice_layer(layer)[1]
+        want_comp[layer * n_tok:(layer + 1) * n_tok] = ob.merge_scatter(
+            layer, hb.pool, want_complete=True)[1]
+        assert ob.gather_objects(layer, hb.pool) == 0
+    assert_bytes_equal(hit_out, want_hit, "hit_out")
+    assert_bytes_equal(complete, want_comp, "complete_out")
+    assert_bytes_equal(d.pool, hb.pool, "pool")
+    assert_bytes_equal(d.objects, hb.objects, "objects")
+    d.pool.fill_(SENT)
+    hb.pool[:] = SENT
+    for l0, k, o in plan_of_launches():
+        gb.scatter_back(l0, d.pool, layer_count=k, **o)
+    for layer in range(L):
+        assert ob.scatter_back(layer, hb.pool) == 0
+    assert_bytes_equal(d.pool, hb.pool, "pool after scatter-back")
+    assert gb.status() == (0, 0)
+
+
 def test_host_legs_with_overlapped_launches():
     """The host-memory variants honour KVL_LAUNCH_OVERLAP_PREVIOUS too: successive
     layers read from a pinned host full block, each launch overlapping the one before."""
