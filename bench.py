@@ -697,6 +697,43 @@ def run_gpu(args):
             stream.wait_stream(h2d)
             stream.wait_stream(d2h)
 
+        def link_rates():
+            """The copy engines' rates on this machine for the step's own transfers: inputs
+            in alone, objects out alone, and both at once (GB/s, best of 3)."""
+            def timed(fn):
+                best = None
+                for _ in range(3):
+                    torch.cuda.synchronize(dev)
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    h2d.wait_stream(stream)
+                    d2h.wait_stream(stream)
+                    fn()
+                    stream.wait_stream(h2d)
+                    stream.wait_stream(d2h)
+                    b.record(stream)
+                    torch.cuda.synchronize(dev)
+                    t = a.elapsed_time(b) / 1e3
+                    best = t if best is None else min(best, t)
+                return best
+
+            def up():
+                with torch.cuda.stream(h2d):
+                    second["hit"].copy_(h_hit, non_blocking=True)
+                    second["miss"].copy_(h_miss, non_blocking=True)
+                    second["tables"].copy_(h_tab, non_blocking=True)
+
+            def down():
+                with torch.cuda.stream(d2h):
+                    h_obj[1].copy_(second["objects"], non_blocking=True)
+
+            t_up, t_down = timed(up), timed(down)
+            t_both = timed(lambda: (up(), down()))
+            return {"h2d_gbs": round(h_in / t_up / 1e9, 1), "d2h_gbs": round(h_out / t_down / 1e9, 1),
+                    "both_gbs": round((h_in + h_out) / t_both / 1e9, 1), "floor_ms_per_step":
+                    round(t_both * 1e3, 3)}
+
+        link = link_rates()
         e2e_run(2)
         torch.cuda.synchronize(dev)
         n_e2e = max(3, min(args.e2e_steps, args.steps))
@@ -714,6 +751,8 @@ def run_gpu(args):
         e2e = {"value": round(world * sb * n_e2e / et / 1e9, 2), "unit": UNIT,
                "h2d_bytes_per_step": int(h_in), "d2h_bytes_per_step": int(h_out),
                "steps": n_e2e, "ms_per_step": round(et / n_e2e * 1e3, 3),
+               "link": dict(link, frac_of_floor=round(link["floor_ms_per_step"] /
+                                                      (et / n_e2e * 1e3), 4)),
                "path": "per step: pinned host -> device copies of the full block, miss KV "
                        "and block tables, the step through the C ABI, objects -> pinned host; "
                        "two buffer sets, so one step's copies overlap its neighbours' kernels"}
