@@ -1,6 +1,6 @@
 """Host logic of bench.py, on the CPU: the algorithmic byte counts behind every GB/s
 figure, the launch-flag rule that decides which launches may overlap, the traffic
-record lookup and the reference arm's JSON line."""
+record lookup, the threaded CPU-oracle harness and the reference arm's JSON line."""
 from __future__ import annotations
 
 import contextlib
@@ -99,3 +99,27 @@ def test_reference_arm_prints_one_json_line():
     assert d["e2e"] == {"value": d["value"], "unit": bench.UNIT, "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
     assert d["config"]["workload"] == "tiny"
+
+
+def test_cpu_baseline_times_the_oracle_on_several_threads():
+    spec = workloads.get_spec("tiny")
+    cpu = bench.cpu_baseline(spec, budget_s=0.2, threads=2)
+    assert cpu["kind"] == "oracle" and cpu["unit"] == bench.UNIT
+    assert cpu["value"] > 0 and cpu["single_thread_value"] > 0
+    assert 1 <= cpu["cores"] <= 2 and cpu["cores_available"] >= cpu["cores"]
+
+
+def test_oracle_workers_share_inputs_and_own_their_outputs():
+    spec = workloads.get_spec("tiny")
+    sample = bench.OracleSample(spec)
+    a, b = bench.oracle_workers(sample, 2)
+    assert a.hit is b.hit and a.miss is b.miss
+    assert a.pool is not b.pool and a.objects is not b.objects
+    # every layer done once, whatever the thread count
+    nbytes, _, layers = bench.time_oracle([a, b], range(spec.L), float("inf"))
+    assert layers == spec.L and nbytes == spec.L * sum(bench.op_bytes(spec).values())
+    # each worker's pool holds what one worker alone computes for the same layer
+    c = bench.oracle_workers(bench.OracleSample(spec), 1)[0]
+    a.run(spec.L - 1)
+    c.run(spec.L - 1)
+    assert (a.pool == c.pool).all() and (a.objects == c.objects).all()
