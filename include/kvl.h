@@ -131,7 +131,8 @@ typedef struct kvl_launch {
  * The caller guarantees that the call touches no byte that the kernels it may overlap
  * write, and writes no byte that they read: the kernel just before it and, when that
  * call carried the flag too, the kernels that call may overlap in turn.  Reads of the
- * same plan, requests and tables are fine.  A call for the same plan, layer and op as
+ * same plan, requests and tables are fine, but the plan's own kernels write the plan:
+ * the first copy call after kvl_batch_plan must not carry the flag.  A call for the same plan, layer and op as
  * the kernel before it must not carry the flag (the two would share a work counter).
  * A call that overlaps a failing one may still copy: the failure shows in the plan's
  * status (kvl_read_status) once both have finished. */
