@@ -536,7 +536,7 @@ def run_gpu(args):
     spec = bench_spec(args)
     bs = BenchStep(spec, dev, layers_per_launch=args.layers_per_launch,
                    serial=args.serial_launches)
-    bufs, lay, g, batch, pool = bs.bufs, bs.bufs["layout"], bs.geom, bs.batch, bs.pool
+    bufs, lay, g, batch = bs.bufs, bs.bufs["layout"], bs.geom, bs.batch
     K, groups, ring, one_layer = bs.K, bs.groups, bs.ring, bs.one_layer
     launch_flags = bs.flags
     stream = torch.cuda.current_stream(dev)

@@ -11,7 +11,7 @@ import torch
 import oracle
 import workloads
 from layer_wise_paged_gb300.batch import MappedHost
-from tests._host import GUARD, geom_of
+from tests._host import GUARD
 
 
 def mapped_copy(a: np.ndarray):

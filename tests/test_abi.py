@@ -8,7 +8,6 @@ import re
 import subprocess
 from pathlib import Path
 
-import numpy as np
 import pytest
 
 import layer_wise_paged_gb300 as kvl

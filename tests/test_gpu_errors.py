@@ -16,7 +16,7 @@ import torch
 import layer_wise_paged_gb300 as kvl
 import oracle
 import workloads
-from tests._device import device_batch, to_dev
+from tests._device import device_batch
 from tests._host import geom_of, host_buffers
 
 pytestmark = pytest.mark.gpu

@@ -20,7 +20,7 @@ import pytest
 
 import oracle
 import workloads
-from tests._host import GUARD, decode_rows, geom_of, host_buffers, tag
+from tests._host import decode_rows, geom_of, host_buffers, tag
 
 SENT = workloads.SENTINEL
 GOLDEN = Path(__file__).resolve().parent / "golden"
