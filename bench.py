@@ -44,6 +44,7 @@ DEFAULT_WORKLOAD = "llama3_8b_agentic"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, vendor figure (context for "% of peak")
 HIT_RING = 8
+KERNEL_REPS = 11  # replays whose per-phase events give the per-kernel median
 OPS = ("slice", "merge_scatter", "gather", "scatter_back")
 KERNEL_NAMES = {"slice": "kvl_slice_kernel", "merge_scatter": "kvl_merge_scatter_kernel",
                 "gather": "kvl_gather_kernel", "scatter_back": "kvl_scatter_back_kernel"}
@@ -602,20 +603,33 @@ def run_gpu(args):
     code, detail = batch.status(stream)
     if code != 0:
         raise SystemExit(f"bench.py: status {code} detail {detail} after the timed steps")
-    # per-launch durations: each op's phase time over its launches; the graph's events
-    # hold the last timed step, eager mode keeps every timed step
-    ev_used = {op: [ev[op]] for op in OPS} if graph is not None else eager_ev
+    # per-launch durations: each op's phase time over its launches, the median over
+    # timed steps.  Eager mode keeps every timed step's events; a graph's events hold
+    # its last replay, so after the timed region the graph is replayed KERNEL_REPS more
+    # times, each read back on its own (these replays are not part of `value`).
+    if graph is not None:
+        phase_s = {op: [] for op in OPS}
+        for _ in range(KERNEL_REPS):
+            graph.replay()
+            torch.cuda.synchronize(dev)
+            for op in OPS:
+                phase_s[op].append(ev[op][0].elapsed_time(ev[op][1]) / 1e3)
+        code, detail = batch.status(stream)
+        if code != 0:
+            raise SystemExit(f"bench.py: status {code} detail {detail} after the timing replays")
+    else:
+        phase_s = {op: [a.elapsed_time(b) / 1e3 for a, b in eager_ev[op]] for op in OPS}
 
     sb = step_bytes(spec)
     value = world * sb * args.steps / elapsed / 1e9
     per_op = {}
     for op in OPS:
-        ts = [a.elapsed_time(b) / 1e3 / len(groups) for a, b in ev_used[op]]
-        avg = sum(ts) / len(ts)
+        ts = [t / len(groups) for t in phase_s[op]]
+        avg = statistics.median(ts)
         per_op[op] = {"us_per_launch": round(avg * 1e6, 2),
                       "gbs": round(op_bytes(spec)[op] * spec.L / len(groups) / avg / 1e9, 1),
                       "layers_per_s": round(spec.L / len(groups) / avg, 1),
-                      "total_s": sum(ts)}
+                      "total_s": avg * len(groups)}
     dom = max(OPS, key=lambda o: per_op[o]["total_s"])
     peak, peak_kind = hbm_peak()
     achieved = per_op[dom]["gbs"]
@@ -773,8 +787,10 @@ def run_gpu(args):
                    launch="CUDA graph of one step, replayed per step" if graph is not None
                    else "eager C-ABI calls from Python",
                    kernel_timing="CUDA events around each op's phase of launches (launch "
-                   "duration = phase time / launches), last timed step" if graph is not None
-                   else "CUDA events around each op's phase of launches, every timed step",
+                   f"duration = phase time / launches), median of {KERNEL_REPS} graph replays "
+                   "after the timed region" if graph is not None
+                   else "CUDA events around each op's phase of launches, median over the "
+                   "timed steps",
                    launch_overlap="none: every launch waits for the one before it"
                    if args.serial_launches else
                    "as below, except gather and scatter-back (shared object layer), "
