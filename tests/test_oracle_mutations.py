@@ -47,6 +47,17 @@ MUTATIONS = {
         "if (seen[b]) {", "if (0) {"),
     "hit_prefix_sum_includes_miss": (
         "hit_off[r + 1] = hit_off[r] + th;", "hit_off[r + 1] = hit_off[r] + th + tm;"),
+    "hit_slot_term_dropped": (
+        "return q->hit_src + blk * q->hit_block_stride + s * q->hit_token_stride",
+        "return q->hit_src + blk * q->hit_block_stride"),
+    "hit_rows_of_previous_request": (
+        "memcpy(complete_out + (row0 + t) * R, hit_layer + (hit0 + t) * R, (size_t)R);",
+        "memcpy(complete_out + (row0 + t) * R, hit_layer + t * R, (size_t)R);"),
+    "gather_reads_layer_zero": (
+        "memcpy(obj, pool_slot(g, (uint8_t *)pool, layer, p, b, 0), (size_t)obj_bytes);",
+        "memcpy(obj, pool_slot(g, (uint8_t *)pool, 0, p, b, 0), (size_t)obj_bytes);"),
+    "scatter_uses_block_index_not_table": (
+        "int64_t b = tables[tab0 + t / g->B];", "int64_t b = (tab0 + t / g->B) % g->n_pool;"),
 }
 
 PIN_CALLS = [
@@ -92,4 +103,7 @@ def test_pins_catch_planted_mistake(tmp_path, name):
             fn(**kw, lib=lib)
         except AssertionError:
             caught.append(fn.__name__)
-    assert caught, f"no pin caught mutation {name}"
+    # the brute-force restatement is a second implementation, not a pin to the pages:
+    # some pin besides it has to see the mistake
+    assert set(caught) - {"test_oracle_matches_brute_force"}, \
+        f"no pin other than the brute force caught mutation {name} ({caught})"
