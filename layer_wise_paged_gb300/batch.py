@@ -69,6 +69,11 @@ class Batch:
     hit, miss, objects: torch uint8 device tensors the layouts' offsets index (or
     None).  tables: int32 device tensor of the packed block tables.  src_tables:
     int32 device tensor of packed full-block tables, or None.
+
+    The copy calls take `layer_count` (layers per launch), `max_ctas` (at most that
+    many SMs) and `flags`, the KVL_LAUNCH_* bits of include/kvl.h: host-memory
+    sources or destinations, KVL_LAUNCH_OVERLAP_PREVIOUS (may run beside the launch
+    before it, which must touch other bytes) and KVL_LAUNCH_SHARE_SMS.
     """
 
     def __init__(self, g, requests, hit, miss, objects, tables, src_tables=None):
