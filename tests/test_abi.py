@@ -65,6 +65,20 @@ int main(void) {{
         assert int(got[f]) == kvl.REQUEST_DTYPE.fields[f][1], f
 
 
+def test_header_constants_match_the_binding():
+    """Every #define KVL_<NAME> <integer> of the header has the same value in the binding."""
+    text = re.sub(r"/\*.*?\*/", "", HEADER.read_text(), flags=re.S)
+    defines = {}
+    for m in re.finditer(r"#define[ \t]+(KVL_[A-Z_]+)[ \t]+(\S.*)", text):
+        expr = m.group(2).strip()
+        assert re.fullmatch(r"[0-9x()<< ]+", expr), (m.group(1), expr)
+        defines[m.group(1)] = eval(expr, {"__builtins__": {}})  # digits, shifts, parentheses
+    assert {"KVL_OK", "KVL_ETIMEOUT", "KVL_LAUNCH_OVERLAP_PREVIOUS", "KVL_LAUNCH_SHARE_SMS",
+            "KVL_STATIC_SCRATCH_POOL_BLOCKS"} <= set(defines)
+    for name, value in defines.items():
+        assert getattr(kvl, name) == value, name
+
+
 def test_plan_layout_is_consistent(lib):
     for L, n, N in [(1, 0, 1), (2, 1, 32), (61, 16, 10625), (32, 256, 49262), (80, 1000, 1 << 20)]:
         g = kvl.geom(L, 2, 16, 256, N)
