@@ -114,7 +114,7 @@ def kvl_plan_bytes(g, n_req: int) -> int:
 
 
 def kvl_plan_layout(g, n_req: int) -> list:
-    off = (ctypes.c_size_t * 10)()
+    off = (ctypes.c_size_t * 11)()
     lib().kvl_plan_layout(_g(g), int(n_req), off)
     return [int(x) for x in off]
 

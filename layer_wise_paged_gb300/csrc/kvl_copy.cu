@@ -56,7 +56,6 @@ enum Op { OP_SLICE = 0, OP_MERGE = 1, OP_GATHER = 2, OP_SCATTER = 3 };
 // of each of two consecutive launches fits on one SM: while one launch drains its last
 // items, the next one's CTAs already stream, and two CTAs per SM together keep as many
 // bytes in flight as one deep CTA.
-constexpr int kStageBytes = 32 * 1024;
 constexpr int kDeepStages = 6;
 constexpr int kShallowStages = 3;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per mbarrier wait

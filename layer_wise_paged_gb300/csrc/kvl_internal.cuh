@@ -30,8 +30,10 @@ struct PlanHeader {
     unsigned long long detail[8];  // 64: per status code, smallest detail recorded
     const void *reqs;            // 128: the request array the plan was built from
     const void *tables;          // 136: the block tables the plan was built from
+    int32_t map_chunk;           // 144: bytes per chunk of a tensor-map row (0: no maps)
+    int32_t pad0;                // 148
 };
-static_assert(sizeof(PlanHeader) == 144, "plan header layout");
+static_assert(sizeof(PlanHeader) == 152, "plan header layout");
 static_assert(sizeof(kvl_request) == 112, "kvl_request layout");
 
 __host__ __device__ inline size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -55,7 +57,11 @@ struct ItemRec {
     int32_t n_hit;        // 23: slots that are hit tokens
     int32_t n_valid;      // 24: slots that are tokens (T_all - j*B, at most B)
     int32_t req;          // 25
-    int32_t pad[6];       // 26
+    int32_t hit_blk_crd;  // 26: block coordinate of the hit rows in the request's hit map
+    int32_t hit_tok_crd;  // 27: token coordinate of slot 0 in the hit map
+    int32_t miss_tok_crd; // 28: token coordinate of slot 0 in the miss map (j*B - T_hit)
+    int32_t map_flags;    // 29: kMap* bits: which of the request's tensor maps exist
+    int32_t pad[2];       // 30
 };
 static_assert(sizeof(ItemRec) == 128, "item record layout");
 
@@ -67,9 +73,53 @@ struct ClaimCounter {
 
 constexpr size_t kRecordsOffset = 256;  // the item records start right after the header
 
+// Shared-memory stage of the copy kernels: one segment of rows, at most this long.
+constexpr int kStageBytes = 32 * 1024;
+
+// Tensor maps.  A request's strided row sources (its hit rows, read a plane at a time
+// by the merge-scatter or a whole row at a time by the slice, and its miss rows) are
+// also described by tensor maps that the plan builds on the device, so that a
+// segment of rows from one source is one tiled bulk-tensor load instead of one bulk
+// load per row.  Each map is a 5-D view of the source with 8-byte elements:
+//   dim 0  bytes of one chunk of a token row (map_chunk / 8 elements)
+//   dim 1  chunks of the token row (R / map_chunk of them; plane p starts at chunk
+//          p * Rp / map_chunk)
+//   dim 2, dim 3  tokens and layers, the one with the smaller stride first
+//   dim 4  full blocks of a block-table source (extent 1 otherwise)
+// The box is one plane row (merge, miss) or one token row (slice) wide and as many
+// token rows high as a segment holds, so its bytes land in the stage as the per-row
+// loads would place them.  Extents are exactly the rows the request declares, so no
+// coordinate reaches memory the per-row loads could not.
+constexpr int kMapBytes = 128;
+constexpr int kMapsPerReq = 3;
+enum MapKind { MAP_HIT = 0, MAP_SLICE = 1, MAP_MISS = 2 };
+constexpr int32_t kMapHit = 1;           // record flag: the request's MAP_HIT exists
+constexpr int32_t kMapSlice = 2;         // MAP_SLICE exists
+constexpr int32_t kMapMiss = 4;          // MAP_MISS exists
+constexpr int32_t kMapHitLayerFirst = 8;   // hit maps order dims 2, 3 as (layer, token)
+constexpr int32_t kMapMissLayerFirst = 16; // miss map orders dims 2, 3 as (layer, token)
+
+// Bytes per chunk of a tensor-map row for plane rows of Rp bytes: the largest
+// multiple of 16 that divides Rp and is at most 2 KiB (a box row holds at most 256
+// elements of 8 bytes).
+__host__ __device__ inline int32_t map_chunk_bytes(int32_t Rp)
+{
+    for (int32_t c = (Rp < 2048 ? Rp : 2048) & ~15; c >= 16; c -= 16)
+        if (Rp % c == 0) return c;
+    return 0;
+}
+
+// Token rows per segment of an op whose rows are `row_bytes` wide: a whole block,
+// or as many rows as a stage holds.
+__host__ __device__ inline int32_t segment_rows(int32_t B, int32_t row_bytes)
+{
+    const int32_t m = kStageBytes / row_bytes;
+    return B < m ? B : m;
+}
+
 // Byte offsets of the plan's sections (see kvl_plan_layout).
 struct PlanLayout {
-    size_t off[10];
+    size_t off[11];
     __host__ __device__ PlanLayout() {}
 };
 
@@ -90,7 +140,10 @@ __host__ __device__ inline PlanLayout plan_layout(int32_t n_req, int64_t pool_bl
     p.off[1] = p.off[7] + round256(L * kOps * sizeof(ClaimCounter)); // tok_off
     p.off[2] = p.off[1] + round256(n1 * 8);                          // hit_off
     p.off[3] = p.off[2] + round256(n1 * 8);                          // blk_off
-    p.off[8] = p.off[3] + round256(n1 * 8);                          // bitmap
+    // tensor maps: kMapsPerReq per request, plus slack to start them on a 128-byte
+    // boundary (the plan itself need only be 16-byte aligned)
+    p.off[10] = p.off[3] + round256(n1 * 8);                         // tensor maps
+    p.off[8] = p.off[10] + round256((n1 - 1) * kMapsPerReq * kMapBytes + kMapBytes);  // bitmap
     p.off[9] = p.off[8] + round256(((cap + 31) / 32) * 4);           // end
     return p;
 }
@@ -106,6 +159,7 @@ struct PlanView {
     ItemRec *items;
     ClaimCounter *counters;  // [L][kOps]
     uint32_t *bitmap;
+    uint8_t *maps;           // [n_req][kMapsPerReq] tensor maps, 128-byte aligned
 };
 
 __host__ __device__ inline PlanView plan_view(void *d_plan, int32_t n_req, int64_t pool_blocks,
@@ -123,6 +177,8 @@ __host__ __device__ inline PlanView plan_view(void *d_plan, int32_t n_req, int64
     v.items = reinterpret_cast<ItemRec *>(b + l.off[6]);
     v.counters = reinterpret_cast<ClaimCounter *>(b + l.off[7]);
     v.bitmap = reinterpret_cast<uint32_t *>(b + l.off[8]);
+    v.maps = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(b + l.off[10]) + 127) &
+                                         ~uintptr_t(127));
     return v;
 }
 
