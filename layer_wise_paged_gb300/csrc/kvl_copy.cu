@@ -86,6 +86,12 @@ struct ItemMeta {
     int64_t dst_pstride;   // bytes between planes, destination side
     int32_t n_a;           // rows (slots) served by src_a
     int32_t n_valid;       // rows (slots) that exist
+    // Tensor maps of the two sources (null: per-row loads), with the coordinates of
+    // slot 0 and the dim order of each (slice and merge-scatter only).
+    const uint8_t *map_a;
+    const uint8_t *map_b;
+    int32_t blk_a, tok_a, tok_b;
+    bool layer_first_a, layer_first_b;
 };
 
 // ---- PTX wrappers ----------------------------------------------------------
@@ -167,6 +173,26 @@ __device__ __forceinline__ void bulk_load(uint32_t dst_smem, const void *src, ui
             dst_smem),
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
+}
+
+// One box of a 5-D tensor map (coordinates innermost first) into shared memory,
+// completing on the stage's mbarrier like bulk_load.
+__device__ __forceinline__ void tensor_load_5d(uint32_t dst_smem, const void *map, int32_t c0,
+                                               int32_t c1, int32_t c2, int32_t c3, int32_t c4,
+                                               uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst_smem),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
+        : "memory");
+}
+
+// The plan wrote its tensor maps with generic stores and a release to the tensor-map
+// proxy; this is the matching acquire, before the first tensor load through `map`.
+__device__ __forceinline__ void acquire_tensor_map(const void *map)
+{
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
 }
 
 __device__ __forceinline__ void bulk_store(void *dst, uint32_t src_smem, uint32_t bytes)
@@ -315,7 +341,8 @@ __device__ __forceinline__ bool plan_usable(const CopyArgs &a)
 {
     PlanHeader *h = static_cast<PlanHeader *>(a.plan);
     if (h->magic != kPlanMagic || h->pool_blocks != a.N || h->block_tokens != a.B ||
-        h->n_layers != a.L || h->reqs != a.reqs || (OP != OP_SLICE && h->tables != a.tables)) {
+        h->n_layers != a.L || h->n_planes != a.P || h->plane_row_bytes != a.Rp ||
+        h->reqs != a.reqs || (OP != OP_SLICE && h->tables != a.tables)) {
         if (blockIdx.x == 0 && threadIdx.x == 0) record_error(h, KVL_EINVAL, 0);
         return false;
     }
@@ -334,8 +361,9 @@ __device__ __forceinline__ uint64_t rec_u64(uint32_t rec, int w)
 // from the item's record.  False (after recording the error) when this op cannot
 // copy the item.
 template <int OP>
-__device__ __forceinline__ bool item_meta(const CopyArgs &a, PlanHeader *h, uint32_t rec, int64_t l,
-                                          int64_t n_hit_all, int64_t n_tok_all, ItemMeta &m)
+__device__ __forceinline__ bool item_meta(const CopyArgs &a, PlanHeader *h, const uint8_t *maps,
+                                          uint32_t rec, int64_t l, int64_t n_hit_all,
+                                          int64_t n_tok_all, ItemMeta &m)
 {
     const int64_t B = a.B, Rp = a.Rp;
     const int64_t lo = l - a.layer;  // output layer within this launch
@@ -356,6 +384,20 @@ __device__ __forceinline__ bool item_meta(const CopyArgs &a, PlanHeader *h, uint
     m.n_a = n_hit;
     m.n_valid = n_valid;
     m.dst2 = nullptr;
+    m.map_a = m.map_b = nullptr;
+    if (OP == OP_SLICE || OP == OP_MERGE) {
+        const int32_t flags = int32_t(rec_word(rec, 29));
+        const uint8_t *req_maps = maps + int64_t(req) * (kMapsPerReq * kMapBytes);
+        const int32_t hit_kind = OP == OP_SLICE ? kMapSlice : kMapHit;
+        if (flags & hit_kind)
+            m.map_a = req_maps + (OP == OP_SLICE ? MAP_SLICE : MAP_HIT) * kMapBytes;
+        if (OP == OP_MERGE && (flags & kMapMiss)) m.map_b = req_maps + MAP_MISS * kMapBytes;
+        m.blk_a = int32_t(rec_word(rec, 26));
+        m.tok_a = int32_t(rec_word(rec, 27));
+        m.tok_b = int32_t(rec_word(rec, 28));
+        m.layer_first_a = (flags & kMapHitLayerFirst) != 0;
+        m.layer_first_b = (flags & kMapMissLayerFirst) != 0;
+    }
     uint8_t *pool_blk = a.pool + ((l * a.P) * a.N + b) * B * Rp;
     const int64_t pool_ps = a.N * B * Rp;
     if (OP == OP_SLICE) {
@@ -454,6 +496,14 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
     const int row_bytes = OP == OP_SLICE ? a.P * a.Rp : a.Rp;
     const int max_rows = kStageBytes / row_bytes;  // >= 1 (host-checked)
     const int64_t R = int64_t(a.P) * a.Rp;
+    // Tensor maps (device buffers only): a segment of box_rows rows from one source
+    // that has a map is one tensor load; plane p starts at chunk p * Rp / chunk.
+    constexpr bool kMaps = HOST == 0 && (OP == OP_SLICE || OP == OP_MERGE);
+    const int32_t map_chunk = kMaps ? h->map_chunk : 0;
+    const uint8_t *maps = map_chunk > 0 ? v.maps : nullptr;
+    const int box_rows = segment_rows(a.B, row_bytes);
+    const int32_t plane_chunks = map_chunk > 0 ? a.Rp / map_chunk : 0;
+    const uint8_t *acquired_a = nullptr, *acquired_b = nullptr;  // lane 0's last acquires
 
     int64_t issued = 0, retired = 0;
     bool timed_out = false;
@@ -534,7 +584,8 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
         if (cur >= n_units || timed_out) break;
 
         ItemMeta m;
-        if (item_meta<OP>(a, h, rec_cur, layer_of(cur), n_hit_all, n_tok_all, m)) {
+        const int64_t l_cur = layer_of(cur);
+        if (item_meta<OP>(a, h, maps, rec_cur, l_cur, n_hit_all, n_tok_all, m)) {
           for (int p = 0; p < planes && !timed_out; ++p) {
             for (int s0 = 0; s0 < m.n_valid && !timed_out; s0 += max_rows) {
                 const int ns = m.n_valid - s0 < max_rows ? m.n_valid - s0 : max_rows;
@@ -581,6 +632,23 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
                 } else if (OP == OP_GATHER || OP == OP_SCATTER) {
                     if (lane == 0)
                         bulk_load(sbase, m.src_a + p * m.src_pstride + int64_t(s0) * row_bytes, bytes, bar);
+                } else if (kMaps && maps && ns == box_rows &&
+                           ((s0 + ns <= m.n_a && m.map_a) || (s0 >= m.n_a && m.map_b))) {
+                    // a whole segment from one mapped source: one box
+                    if (lane == 0) {
+                        const bool from_a = s0 + ns <= m.n_a;
+                        const uint8_t *map = from_a ? m.map_a : m.map_b;
+                        const uint8_t *&acq = from_a ? acquired_a : acquired_b;
+                        if (map != acq) {
+                            acquire_tensor_map(map);
+                            acq = map;
+                        }
+                        const int32_t tok = (from_a ? m.tok_a : m.tok_b) + s0;
+                        const int32_t lay = int32_t(l_cur);
+                        const bool lf = from_a ? m.layer_first_a : m.layer_first_b;
+                        tensor_load_5d(sbase, map, 0, OP == OP_MERGE ? p * plane_chunks : 0,
+                                       lf ? lay : tok, lf ? tok : lay, from_a ? m.blk_a : 0, bar);
+                    }
                 } else {
                     for (int i = lane; i < ns; i += 32) {
                         const int64_t s = s0 + i;

@@ -31,9 +31,11 @@ struct PlanHeader {
     const void *reqs;            // 128: the request array the plan was built from
     const void *tables;          // 136: the block tables the plan was built from
     int32_t map_chunk;           // 144: bytes per chunk of a tensor-map row (0: no maps)
-    int32_t pad0;                // 148
+    int32_t n_planes;            // 148: P the plan was built for
+    int32_t plane_row_bytes;     // 152: Rp the plan was built for
+    int32_t pad0;                // 156
 };
-static_assert(sizeof(PlanHeader) == 152, "plan header layout");
+static_assert(sizeof(PlanHeader) == 160, "plan header layout");
 static_assert(sizeof(kvl_request) == 112, "kvl_request layout");
 
 __host__ __device__ inline size_t round256(size_t x) { return (x + 255) & ~size_t(255); }

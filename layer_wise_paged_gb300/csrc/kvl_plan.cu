@@ -337,6 +337,8 @@ __global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(PlanArgs a)
         h->reqs = a.reqs;
         h->tables = a.tables;
         h->map_chunk = a.map_ops ? a.map_chunk : 0;
+        h->n_planes = a.P;
+        h->plane_row_bytes = a.Rp;
         h->pad0 = 0;
         h->magic = kPlanMagic;
     }
@@ -443,7 +445,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 }
 
 // A map a plan's tensor maps start from: rank 5, 8-byte elements, no interleave or
-// swizzle, L2 promotion in 256-byte lines, zero fill out of bounds, and the box of
+// swizzle, L2 promotion in 128-byte lines, zero fill out of bounds, and the box of
 // `rows` token rows of W bytes (chunks of C bytes), the rows along dim 2 (token
 // first) or dim 3 (layer first).  Its address, dims and strides are placeholders
 // that the fill kernel replaces; it spans kTemplateSpan bytes along dim 4, as
@@ -465,7 +467,7 @@ bool encode_template(CUtensorMap *t, void *addr, int32_t C, int32_t R, int32_t W
     const cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
     return enc(t, CU_TENSOR_MAP_DATA_TYPE_UINT64, 5, addr, dims, strides, box, elem_strides,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // The maps a geometry allows (a box is at most 256 elements along each dim, and a

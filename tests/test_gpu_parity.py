@@ -126,6 +126,41 @@ def test_random_ragged_batches_bit_exact(case):
     run_parity(spec)
 
 
+MAPPED_CASES = 16
+
+
+@pytest.mark.parametrize("case", range(MAPPED_CASES))
+def test_random_ragged_batches_through_tensor_maps(case):
+    """Ragged batches whose sources are large enough (a dim spanning 1 MiB or more)
+    for the plan's tensor maps, so whole segments go through tiled tensor loads and
+    the rest (hit/miss boundary blocks, partial last blocks, short segments) through
+    per-row loads, side by side in one launch."""
+    g = np.random.default_rng(9500 + case)
+    P = int(g.integers(1, 3))
+    Rp = int(g.choice([256, 1152, 2048, 4096]))
+    B = int(g.choice([3, 16, 64]))
+    L = int(g.integers(2, 5))
+    n = int(g.choice([1, 3, 6]))
+    R = P * Rp
+    lo = -(-(1 << 20) // ((L - 1) * R)) + 1   # enough tokens for a 1 MiB hit span
+    t_hit = g.integers(lo, 3 * lo, n)
+    t_miss = g.integers(lo // 2, 2 * lo, n)
+    if case % 4 == 0:
+        t_miss[0] = int(g.integers(0, 3))   # hit blocks end inside a block
+    spec = workloads.custom_spec(
+        L=L, P=P, B=B, Rp=Rp, t_hit=t_hit, t_miss=t_miss,
+        table=str(g.choice(["perm", "fragmented"])),
+        source=str(g.choice(["contiguous", "permuted"])),
+        miss_order=str(g.choice(["layer", "token"])), seed=950 + case,
+        objects=str(g.choice(["layer", "block"])))
+    hb = host_buffers(spec)
+    gb, _ = device_batch(spec, hb)
+    gb.plan()
+    flags = gb.d_plan.cpu().numpy()[256:256 + 128 * gb.n_items].view(np.int32).reshape(-1, 32)[:, 29]
+    assert (flags & 1).any() and (flags & 2).any(), "no hit maps were built"
+    run_parity(spec)
+
+
 SCALED = {
     # the shapes of the four larger workloads, with fewer layers and tokens
     "llama3_8b_agentic": dict(L=3, P=2, B=16, Rp=2048, t_hit=[3000], t_miss=[77], table="perm"),

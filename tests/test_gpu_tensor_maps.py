@@ -149,8 +149,8 @@ def host_encode(base, dims, strides, box):
     addr = (ctypes.addressof(raw) + 63) & ~63   # a tensor map is 64-byte aligned
     u64, u32 = ctypes.c_uint64, ctypes.c_uint32
     rc = _encode(addr, 4, 5, base, (u64 * 5)(*dims), (u64 * 4)(*strides), (u32 * 5)(*box),
-                 (u32 * 5)(1, 1, 1, 1, 1), 0, 0, 3, 0)  # UINT64; no interleave or swizzle;
-    assert rc == 0, f"cuTensorMapEncodeTiled failed ({rc})"  # L2 promotion 256 B; zero fill
+                 (u32 * 5)(1, 1, 1, 1, 1), 0, 0, 2, 0)  # UINT64; no interleave or swizzle;
+    assert rc == 0, f"cuTensorMapEncodeTiled failed ({rc})"  # L2 promotion 128 B; zero fill
     return np.frombuffer(ctypes.string_at(addr, 128), np.uint8)
 
 
