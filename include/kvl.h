@@ -176,7 +176,8 @@ size_t kvl_plan_bytes(const kvl_geom *geom, int32_t n_req);
  * off[5] item_blk (int32[pool_blocks]), off[6] item records (always at byte 256),
  * off[7] claim counters, off[8] injectivity bitmap (the last section), off[9] total
  * bytes, off[10] tensor maps (3 x 128 bytes per request, starting at the first
- * 128-byte boundary at or after the plan's address + off[10]).  Sections are not
+ * 128-byte boundary at or after the plan's address + off[10], then an int32 of map
+ * flags per request).  Sections are not
  * placed in index order.  The header's first int32 is the status and its int64 at
  * byte 16 the item count. */
 void kvl_plan_layout(const kvl_geom *geom, int32_t n_req, size_t off[11]);

@@ -143,9 +143,10 @@ __host__ __device__ inline PlanLayout plan_layout(int32_t n_req, int64_t pool_bl
     p.off[2] = p.off[1] + round256(n1 * 8);                          // hit_off
     p.off[3] = p.off[2] + round256(n1 * 8);                          // blk_off
     // tensor maps: kMapsPerReq per request, plus slack to start them on a 128-byte
-    // boundary (the plan itself need only be 16-byte aligned)
+    // boundary (the plan itself need only be 16-byte aligned), then each request's
+    // map flags (int32)
     p.off[10] = p.off[3] + round256(n1 * 8);                         // tensor maps
-    p.off[8] = p.off[10] + round256((n1 - 1) * kMapsPerReq * kMapBytes + kMapBytes);  // bitmap
+    p.off[8] = p.off[10] + round256((n1 - 1) * (kMapsPerReq * kMapBytes + 4) + kMapBytes);  // bitmap
     p.off[9] = p.off[8] + round256(((cap + 31) / 32) * 4);           // end
     return p;
 }
@@ -162,6 +163,7 @@ struct PlanView {
     ClaimCounter *counters;  // [L][kOps]
     uint32_t *bitmap;
     uint8_t *maps;           // [n_req][kMapsPerReq] tensor maps, 128-byte aligned
+    int32_t *map_flags;      // [n_req] kMap* flags of each request, after the maps
 };
 
 __host__ __device__ inline PlanView plan_view(void *d_plan, int32_t n_req, int64_t pool_blocks,
@@ -181,6 +183,7 @@ __host__ __device__ inline PlanView plan_view(void *d_plan, int32_t n_req, int64
     v.bitmap = reinterpret_cast<uint32_t *>(b + l.off[8]);
     v.maps = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(b + l.off[10]) + 127) &
                                          ~uintptr_t(127));
+    v.map_flags = reinterpret_cast<int32_t *>(v.maps + size_t(n_req < 0 ? 0 : n_req) * kMapsPerReq * kMapBytes);
     return v;
 }
 

@@ -231,7 +231,7 @@ __device__ void build_maps(const PlanArgs &a)
     for (int64_t r = int64_t(blockIdx.x) * kWarps + warp; r < a.n_req; r += n_warps) {
         const kvl_request q = a.reqs[r];
         MapShape sh[kMapsPerReq];
-        const int32_t flags = request_maps(a, q, sh);
+        const int32_t flags = request_maps(a, q, sh);  // = map_flags[r], with the shapes
         for (int k = 0; k < kMapsPerReq; ++k) {
             if (!(flags & (1 << k))) continue;  // kMapHit, kMapSlice, kMapMiss = bit MapKind
             const uint4 *tmpl = reinterpret_cast<const uint4 *>(
@@ -273,6 +273,9 @@ __global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(PlanArgs a)
         if (r < a.n_req) {
             const kvl_request q = a.reqs[r];
             const int code = validate_request(q);
+            // the request's tensor maps (the fill kernel builds them and stamps these
+            // flags into the request's item records); none for an invalid request
+            a.v.map_flags[r] = code ? 0 : request_maps(a, q, nullptr);
             if (code) {
                 atomicMax(&s_code, code);
                 atomicMin(&s_detail[code], (unsigned long long)r);
@@ -419,7 +422,7 @@ __global__ void __launch_bounds__(kFillThreads) plan_fill_kernel(const __grid_co
         rec.hit_blk_crd = q.hit_src_table ? int32_t(sb) : 0;
         rec.hit_tok_crd = q.hit_src_table ? 0 : int32_t(t0);
         rec.miss_tok_crd = int32_t(t0 - t_hit);
-        rec.map_flags = request_maps(a, q, nullptr);
+        rec.map_flags = a.v.map_flags[r];
         rec.pad[0] = rec.pad[1] = 0;
         a.v.items[i] = rec;
     }
