@@ -258,7 +258,8 @@ kvl_status kvl_batch_plan_static_scratch(const kvl_geom *geom, int32_t n_req,
  * kvl_plan_layout(geom, 0)[8] bytes (true of any plan kvl_batch_plan accepted for it).
  * The kernels read its item records before they check the header, so a buffer
  * sized for a smaller pool may be read past its end; a plan built for other arrays or
- * another geometry that is large enough is refused (KVL_EINVAL in its status).
+ * another geometry (L, P, B, Rp or N) that is large enough is refused (KVL_EINVAL in
+ * its status).
  * d_reqs and d_block_tables are the arrays the plan was built from; NULL only if it was
  * built from NULL (a batch of no requests); other NULLs are refused on the device. */
 

@@ -17,10 +17,12 @@
 //     strides at layer 0, pool block id, hit / valid slot counts); the warp loads the
 //     next item's record (one word per lane) while the current item's copies run,
 //     and reads fields from their lanes with shuffles;
-//   * loads: `cp.async.bulk` global -> shared, one per source row (a token's plane is
-//     not adjacent to the next token's in the full-block source), or one per segment
-//     when the source run is contiguous (gather / scatter-back), completing on the
-//     stage's mbarrier;
+//   * loads, completing on the stage's mbarrier: a segment of strided rows (a token's
+//     plane is not adjacent to the next token's in the full-block source) is one tiled
+//     `cp.async.bulk.tensor` load through the plan's tensor map of its source when it
+//     is a whole segment drawn from one mapped source, else one `cp.async.bulk` load
+//     per row; a contiguous source run (gather / scatter-back) is one `cp.async.bulk`
+//     load per segment;
 //   * stores: one `cp.async.bulk` shared -> global per segment (a segment is a run of
 //     slots of one item and plane, at most one stage long, whose destination is
 //     contiguous), in bulk groups; a stage is refilled only after its store has read

@@ -175,6 +175,18 @@ def test_host_side_checks_return_without_launching():
     other = kvl.geom(SPEC.L, SPEC.P, SPEC.B, SPEC.Rp, SPEC.n_pool - 1)
     assert kvl.kvl_merge_scatter_paged(other, plan, reqs, tabs, 0, 1, pool, None, None, s) == kvl.KVL_OK
     assert gb.status()[0] == kvl.KVL_EINVAL
+    # ... and so is one built for another row size or plane count (the boxes of its
+    # tensor maps hold the plan's rows); the call copies nothing
+    for other in (kvl.geom(SPEC.L, SPEC.P, SPEC.B, SPEC.Rp + 16, SPEC.n_pool),
+                  kvl.geom(SPEC.L, 1, SPEC.B, SPEC.Rp, SPEC.n_pool)):
+        gb.plan()
+        assert gb.status() == (0, 0)
+        before = d.pool.clone()
+        assert kvl.kvl_merge_scatter_paged(other, plan, reqs, tabs, 0, 1, pool, None, None,
+                                           s) == kvl.KVL_OK
+        assert kvl.kvl_slice_layer(other, plan, reqs, 0, 1, pool, None, s) == kvl.KVL_OK
+        assert gb.status()[0] == kvl.KVL_EINVAL
+        assert torch.equal(d.pool, before)
 
 
 def test_a_wait_that_runs_out_reports_a_timeout_and_the_context_survives():
