@@ -175,7 +175,7 @@ size_t kvl_plan_bytes(const kvl_geom *geom, int32_t n_req);
  * off[3] blk_off (int64[n_req+1]), off[4] item_req (int32[pool_blocks]),
  * off[5] item_blk (int32[pool_blocks]), off[6] item records (always at byte 256),
  * off[7] claim counters, off[8] injectivity bitmap (the last section), off[9] total
- * bytes, off[10] tensor maps (3 x 128 bytes per request, starting at the first
+ * bytes, off[10] tensor maps (6 x 128 bytes per request, starting at the first
  * 128-byte boundary at or after the plan's address + off[10], then an int32 of map
  * flags per request).  Sections are not
  * placed in index order.  The header's first int32 is the status and its int64 at
@@ -195,8 +195,9 @@ void kvl_plan_layout(const kvl_geom *geom, int32_t n_req, size_t off[11]);
  * The plan also describes each request's strided row sources (hit rows, miss rows)
  * by tensor maps, built on the device from a template, when their strides lay the
  * rows out without overlap (each stride at least the extent below it); the copy
- * calls then read a segment of rows of one source with one tiled bulk-tensor load
- * instead of one bulk load per row.  The maps span exactly the rows a request
+ * calls then read a segment of rows of one source (a whole segment, or the rows a
+ * block has left after its whole segments) with one tiled bulk-tensor load instead
+ * of one bulk load per row.  The maps span exactly the rows a request
  * declares: T_hit rows of a full block without a table, all B token rows of each
  * of the hit_src_blocks blocks with a table (so with a table every one of those
  * blocks must be whole), and T_miss rows of the miss KV, each over all L layers.

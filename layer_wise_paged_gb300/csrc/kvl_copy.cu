@@ -20,8 +20,8 @@
 //   * loads, completing on the stage's mbarrier: a segment of strided rows (a token's
 //     plane is not adjacent to the next token's in the full-block source) is one tiled
 //     `cp.async.bulk.tensor` load through the plan's tensor map of its source when it
-//     is a whole segment drawn from one mapped source, else one `cp.async.bulk` load
-//     per row; a contiguous source run (gather / scatter-back) is one `cp.async.bulk`
+//     is a whole segment or a block's tail drawn from one mapped source, else one
+//     `cp.async.bulk` load per row; a contiguous source run (gather / scatter-back) is one `cp.async.bulk`
 //     load per segment;
 //   * stores: one `cp.async.bulk` shared -> global per segment (a segment is a run of
 //     slots of one item and plane, at most one stage long, whose destination is
@@ -88,10 +88,10 @@ struct ItemMeta {
     int64_t dst_pstride;   // bytes between planes, destination side
     int32_t n_a;           // rows (slots) served by src_a
     int32_t n_valid;       // rows (slots) that exist
-    // Tensor maps of the two sources (null: per-row loads), with the coordinates of
-    // slot 0 and the dim order of each (slice and merge-scatter only).
-    const uint8_t *map_a;
-    const uint8_t *map_b;
+    // Tensor maps of the two sources, of whole segments and of block tails (null:
+    // per-row loads), with the coordinates of slot 0 and the dim order of each source
+    // (slice and merge-scatter only).
+    const uint8_t *map_a, *map_a_tail, *map_b, *map_b_tail;
     int32_t blk_a, tok_a, tok_b;
     bool layer_first_a, layer_first_b;
 };
@@ -386,14 +386,18 @@ __device__ __forceinline__ bool item_meta(const CopyArgs &a, PlanHeader *h, cons
     m.n_a = n_hit;
     m.n_valid = n_valid;
     m.dst2 = nullptr;
-    m.map_a = m.map_b = nullptr;
-    if (OP == OP_SLICE || OP == OP_MERGE) {
+    m.map_a = m.map_a_tail = m.map_b = m.map_b_tail = nullptr;
+    if (maps && (OP == OP_SLICE || OP == OP_MERGE)) {
         const int32_t flags = int32_t(rec_word(rec, 29));
         const uint8_t *req_maps = maps + int64_t(req) * (kMapsPerReq * kMapBytes);
-        const int32_t hit_kind = OP == OP_SLICE ? kMapSlice : kMapHit;
-        if (flags & hit_kind)
-            m.map_a = req_maps + (OP == OP_SLICE ? MAP_SLICE : MAP_HIT) * kMapBytes;
-        if (OP == OP_MERGE && (flags & kMapMiss)) m.map_b = req_maps + MAP_MISS * kMapBytes;
+        auto map_of = [&](int k) { return (flags & map_bit(k)) ? req_maps + k * kMapBytes : nullptr; };
+        const int hit_kind = OP == OP_SLICE ? MAP_SLICE : MAP_HIT;
+        m.map_a = map_of(hit_kind);
+        m.map_a_tail = map_of(hit_kind + kMapTail);
+        if (OP == OP_MERGE) {
+            m.map_b = map_of(MAP_MISS);
+            m.map_b_tail = map_of(MAP_MISS_TAIL);
+        }
         m.blk_a = int32_t(rec_word(rec, 26));
         m.tok_a = int32_t(rec_word(rec, 27));
         m.tok_b = int32_t(rec_word(rec, 28));
@@ -503,9 +507,11 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
     constexpr bool kMaps = HOST == 0 && (OP == OP_SLICE || OP == OP_MERGE);
     const int32_t map_chunk = kMaps ? h->map_chunk : 0;
     const uint8_t *maps = map_chunk > 0 ? v.maps : nullptr;
-    const int box_rows = segment_rows(a.B, row_bytes);
+    const int box_rows = segment_rows(a.B, row_bytes);        // a whole segment's box
+    const int tail_rows = segment_tail_rows(a.B, row_bytes);  // a block tail's box (0: none)
     const int32_t plane_chunks = map_chunk > 0 ? a.Rp / map_chunk : 0;
-    const uint8_t *acquired_a = nullptr, *acquired_b = nullptr;  // lane 0's last acquires
+    // lane 0's four most recently acquired maps, newest first
+    const uint8_t *acq0 = nullptr, *acq1 = nullptr, *acq2 = nullptr, *acq3 = nullptr;
 
     int64_t issued = 0, retired = 0;
     bool timed_out = false;
@@ -634,17 +640,24 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
                 } else if (OP == OP_GATHER || OP == OP_SCATTER) {
                     if (lane == 0)
                         bulk_load(sbase, m.src_a + p * m.src_pstride + int64_t(s0) * row_bytes, bytes, bar);
-                } else if (kMaps && maps && ns == box_rows &&
-                           ((s0 + ns <= m.n_a && m.map_a) || (s0 >= m.n_a && m.map_b))) {
-                    // a whole segment from one mapped source: one box
+                } else if (const uint8_t *map = !kMaps ? nullptr
+                                                : ns == box_rows
+                                                    ? (s0 + ns <= m.n_a ? m.map_a : s0 >= m.n_a ? m.map_b : nullptr)
+                                                : ns == tail_rows
+                                                    ? (s0 + ns <= m.n_a ? m.map_a_tail
+                                                       : s0 >= m.n_a   ? m.map_b_tail
+                                                                       : nullptr)
+                                                    : nullptr) {
+                    // a whole segment or a block tail from one mapped source: one box
                     if (lane == 0) {
-                        const bool from_a = s0 + ns <= m.n_a;
-                        const uint8_t *map = from_a ? m.map_a : m.map_b;
-                        const uint8_t *&acq = from_a ? acquired_a : acquired_b;
-                        if (map != acq) {
+                        if (map != acq0 && map != acq1 && map != acq2 && map != acq3) {
                             acquire_tensor_map(map);
-                            acq = map;
+                            acq3 = acq2;
+                            acq2 = acq1;
+                            acq1 = acq0;
+                            acq0 = map;
                         }
+                        const bool from_a = s0 + ns <= m.n_a;
                         const int32_t tok = (from_a ? m.tok_a : m.tok_b) + s0;
                         const int32_t lay = int32_t(l_cur);
                         const bool lf = from_a ? m.layer_first_a : m.layer_first_b;

@@ -90,16 +90,26 @@ constexpr int kStageBytes = 32 * 1024;
 //   dim 4  full blocks of a block-table source (extent 1 otherwise)
 // The box is one plane row (merge, miss) or one token row (slice) wide and as many
 // token rows high as a segment holds, so its bytes land in the stage as the per-row
-// loads would place them.  Extents are exactly the rows the request declares, so no
-// coordinate reaches memory the per-row loads could not.
+// loads would place them.  Each source has a map of each of two box heights: a whole
+// segment, and the rows a block has left after its whole segments (its tail: B mod
+// the segment rows, when that is not 0).  Extents are exactly the rows the request
+// declares, so no coordinate reaches memory the per-row loads could not.
 constexpr int kMapBytes = 128;
-constexpr int kMapsPerReq = 3;
-enum MapKind { MAP_HIT = 0, MAP_SLICE = 1, MAP_MISS = 2 };
-constexpr int32_t kMapHit = 1;           // record flag: the request's MAP_HIT exists
-constexpr int32_t kMapSlice = 2;         // MAP_SLICE exists
-constexpr int32_t kMapMiss = 4;          // MAP_MISS exists
-constexpr int32_t kMapHitLayerFirst = 8;   // hit maps order dims 2, 3 as (layer, token)
-constexpr int32_t kMapMissLayerFirst = 16; // miss map orders dims 2, 3 as (layer, token)
+enum MapKind {
+    MAP_HIT = 0,         // hit plane rows (merge-scatter), whole segments
+    MAP_SLICE = 1,       // hit token rows (slice), whole segments
+    MAP_MISS = 2,        // miss plane rows (merge-scatter), whole segments
+    MAP_HIT_TAIL = 3,    // the same three sources, block tails
+    MAP_SLICE_TAIL = 4,
+    MAP_MISS_TAIL = 5,
+};
+constexpr int kMapsPerReq = 6;
+constexpr int kMapTail = MAP_HIT_TAIL - MAP_HIT;  // a kind's tail kind is kind + kMapTail
+// Record flags: bit `kind` says the request's map of that kind exists; the hit maps
+// (and the miss maps) share one view of their source, so one dim order each.
+__host__ __device__ constexpr int32_t map_bit(int kind) { return int32_t(1) << kind; }
+constexpr int32_t kMapHitLayerFirst = 64;   // hit maps order dims 2, 3 as (layer, token)
+constexpr int32_t kMapMissLayerFirst = 128; // miss maps order dims 2, 3 as (layer, token)
 
 // Bytes per chunk of a tensor-map row for plane rows of Rp bytes: the largest
 // multiple of 16 that divides Rp and is at most 2 KiB (a box row holds at most 256
@@ -117,6 +127,13 @@ __host__ __device__ inline int32_t segment_rows(int32_t B, int32_t row_bytes)
 {
     const int32_t m = kStageBytes / row_bytes;
     return B < m ? B : m;
+}
+
+// Rows of a whole block left after its whole segments (0: segments divide blocks).
+__host__ __device__ inline int32_t segment_tail_rows(int32_t B, int32_t row_bytes)
+{
+    const int32_t m = segment_rows(B, row_bytes);
+    return m > 0 ? B % m : 0;
 }
 
 // Byte offsets of the plan's sections (see kvl_plan_layout).

@@ -37,14 +37,24 @@ struct PlanArgs {
     int32_t check_injective;
     int32_t P, Rp, L;
     int32_t map_chunk;  // bytes per chunk of a map row; 0: build no tensor maps
-    int32_t map_ops;    // kMapHit | kMapSlice | kMapMiss: the maps this geometry allows
+    int32_t map_ops;    // map_bit(kind) for every map kind this geometry allows
     // Host-encoded maps that the fill kernel copies and edits, by row width (0: plane
-    // rows, for MAP_HIT and MAP_MISS; 1: token rows, for MAP_SLICE) and dim order (0:
-    // token first; 1: layer first).  Each already has its final box: the encoder
-    // derives more from the box than the box dims themselves, so only the address,
-    // dims and strides are edited on the device.
-    CUtensorMap tmpl[2][2];
+    // rows, for the hit and miss maps; 1: token rows, for the slice maps), dim order
+    // (0: token first; 1: layer first) and box height (0: a whole segment; 1: a block
+    // tail).  Each already has its final box: the encoder derives more from the box
+    // than the box dims themselves, so only the address, dims and strides are edited
+    // on the device.
+    CUtensorMap tmpl[2][2][2];
 };
+
+// Row width, box height and box rows of a map kind.
+__host__ __device__ inline bool kind_token_rows(int kind) { return kind == MAP_SLICE || kind == MAP_SLICE_TAIL; }
+__host__ __device__ inline bool kind_tail(int kind) { return kind >= kMapTail; }
+__host__ __device__ inline int32_t kind_rows(int kind, int32_t B, int32_t P, int32_t Rp)
+{
+    const int32_t w = kind_token_rows(kind) ? P * Rp : Rp;
+    return kind_tail(kind) ? segment_tail_rows(B, w) : segment_rows(B, w);
+}
 
 // Inclusive scan of one int64 across a warp.
 __device__ __forceinline__ int64_t warp_inclusive(int64_t x, int lane)
@@ -152,16 +162,18 @@ __device__ bool map_shape(uint64_t base, int64_t n_tok, int64_t ts, int64_t L, i
     return true;
 }
 
-// The tensor maps request q gets (kMap* flags), and their fields if `shapes` is not
-// null.  Hit rows: with a full-block table, blocks of B token rows (every one of the
-// hit_src_blocks blocks is whole); without one, T_hit token rows when consecutive
-// blocks follow one another (block stride = B x token stride, or a single block).
+// The tensor maps request q gets (map_bit flags and the dim-order flags), and their
+// fields if `shapes` is not null.  Hit rows: with a full-block table, blocks of B
+// token rows (every one of the hit_src_blocks blocks is whole); without one, T_hit
+// token rows when consecutive blocks follow one another (block stride = B x token
+// stride, or a single block).  All maps of one source share its view, so its dim
+// order.
 __device__ int32_t request_maps(const PlanArgs &a, const kvl_request &q, MapShape *shapes)
 {
     if (!a.map_ops) return 0;
-    MapShape tmp[kMapsPerReq];
-    MapShape *sh = shapes ? shapes : tmp;
-    const int32_t C = a.map_chunk, Rp = a.Rp, R = a.P * a.Rp;
+    MapShape scratch;  // the flags alone need no shapes kept
+    auto sh_of = [&](int k) -> MapShape & { return shapes ? shapes[k] : scratch; };
+    const int32_t C = a.map_chunk, R = a.P * a.Rp;
     const int64_t B = a.B;
     int32_t flags = 0;
     if (q.t_hit > 0) {
@@ -175,23 +187,27 @@ __device__ int32_t request_maps(const PlanArgs &a, const kvl_request &q, MapShap
             n_tok = q.t_hit;
             n_blk = 1;
         }
-        if (n_tok > 0) {
-            if ((a.map_ops & kMapHit) &&
+        const int hit_kinds[4] = {MAP_HIT, MAP_SLICE, MAP_HIT_TAIL, MAP_SLICE_TAIL};
+        for (int i = 0; i < 4 && n_tok > 0; ++i) {
+            const int k = hit_kinds[i];
+            MapShape &sh = sh_of(k);
+            if ((a.map_ops & map_bit(k)) &&
                 map_shape(base, n_tok, ts, a.L, q.hit_layer_stride, n_blk, bs, R, C,
-                          segment_rows(a.B, Rp), sh[MAP_HIT]))
-                flags |= kMapHit | (sh[MAP_HIT].layer_first ? kMapHitLayerFirst : 0);
-            // the slice's map has the same view, so the same dim order
-            if ((a.map_ops & kMapSlice) &&
-                map_shape(base, n_tok, ts, a.L, q.hit_layer_stride, n_blk, bs, R, C,
-                          segment_rows(a.B, R), sh[MAP_SLICE]) &&
-                (!(flags & kMapHit) || sh[MAP_SLICE].layer_first == sh[MAP_HIT].layer_first))
-                flags |= kMapSlice | (sh[MAP_SLICE].layer_first ? kMapHitLayerFirst : 0);
+                          kind_rows(k, a.B, a.P, a.Rp), sh))
+                flags |= map_bit(k) | (sh.layer_first ? kMapHitLayerFirst : 0);
         }
     }
-    if (q.t_miss > 0 && (a.map_ops & kMapMiss) &&
-        map_shape(reinterpret_cast<uint64_t>(q.miss_src), q.t_miss, q.miss_token_stride, a.L,
-                  q.miss_layer_stride, 1, 0, R, C, segment_rows(a.B, Rp), sh[MAP_MISS]))
-        flags |= kMapMiss | (sh[MAP_MISS].layer_first ? kMapMissLayerFirst : 0);
+    if (q.t_miss > 0) {
+        const int miss_kinds[2] = {MAP_MISS, MAP_MISS_TAIL};
+        for (int i = 0; i < 2; ++i) {
+            const int k = miss_kinds[i];
+            MapShape &sh = sh_of(k);
+            if ((a.map_ops & map_bit(k)) &&
+                map_shape(reinterpret_cast<uint64_t>(q.miss_src), q.t_miss, q.miss_token_stride,
+                          a.L, q.miss_layer_stride, 1, 0, R, C, kind_rows(k, a.B, a.P, a.Rp), sh))
+                flags |= map_bit(k) | (sh.layer_first ? kMapMissLayerFirst : 0);
+        }
+    }
     return flags;
 }
 
@@ -233,9 +249,9 @@ __device__ void build_maps(const PlanArgs &a)
         MapShape sh[kMapsPerReq];
         const int32_t flags = request_maps(a, q, sh);  // = map_flags[r], with the shapes
         for (int k = 0; k < kMapsPerReq; ++k) {
-            if (!(flags & (1 << k))) continue;  // kMapHit, kMapSlice, kMapMiss = bit MapKind
+            if (!(flags & map_bit(k))) continue;
             const uint4 *tmpl = reinterpret_cast<const uint4 *>(
-                &a.tmpl[k == MAP_SLICE ? 1 : 0][sh[k].layer_first ? 1 : 0]);
+                &a.tmpl[kind_token_rows(k) ? 1 : 0][sh[k].layer_first ? 1 : 0][kind_tail(k) ? 1 : 0]);
             if (lane < kMapBytes / 16) reinterpret_cast<uint4 *>(s_map[warp])[lane] = tmpl[lane];
             __syncwarp();
             if (lane == 0) map_replace(sm, sh[k]);
@@ -473,17 +489,19 @@ bool encode_template(CUtensorMap *t, void *addr, int32_t C, int32_t R, int32_t W
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The maps a geometry allows (a box is at most 256 elements along each dim, and a
-// slice row must fit one stage).
+// The map kinds a geometry allows: a box is at most 256 elements along each dim, a
+// slice row must fit one stage, and a tail kind exists only where blocks have a tail.
 int32_t geometry_map_ops(const kvl_geom *g, int32_t C)
 {
     if (C <= 0) return 0;
     const int64_t Rp = g->plane_row_bytes, R = int64_t(g->n_planes) * Rp;
     int32_t ops = 0;
-    if (Rp / C <= 256 && segment_rows(g->block_tokens, int32_t(Rp)) <= 256 && R / C <= INT32_MAX)
-        ops |= kMapHit | kMapMiss;
-    if (R <= kStageBytes && R / C <= 256 && segment_rows(g->block_tokens, int32_t(R)) <= 256)
-        ops |= kMapSlice;
+    for (int k = 0; k < kMapsPerReq; ++k) {
+        const int64_t w = kind_token_rows(k) ? R : Rp;
+        if (w > kStageBytes || w / C > 256 || R / C > INT32_MAX) continue;
+        const int32_t rows = kind_rows(k, g->block_tokens, g->n_planes, g->plane_row_bytes);
+        if (rows >= 1 && rows <= 256) ops |= map_bit(k);
+    }
     return ops;
 }
 
@@ -505,14 +523,21 @@ PlanArgs plan_args(const kvl_geom *geom, int32_t n_req, const kvl_request *d_req
     a.map_chunk = map_chunk_bytes(geom->plane_row_bytes);
     a.map_ops = geometry_map_ops(geom, a.map_chunk);
     std::memset(&a.tmpl, 0, sizeof(a.tmpl));
-    const int32_t C = a.map_chunk, Rp = a.Rp, R = a.P * a.Rp;
-    for (int order = 0; order < 2; ++order) {
-        if ((a.map_ops & (kMapHit | kMapMiss)) &&
-            !encode_template(&a.tmpl[0][order], d_plan, C, R, Rp, segment_rows(a.B, Rp), order))
-            a.map_ops &= ~(kMapHit | kMapMiss);
-        if ((a.map_ops & kMapSlice) &&
-            !encode_template(&a.tmpl[1][order], d_plan, C, R, R, segment_rows(a.B, R), order))
-            a.map_ops &= ~kMapSlice;
+    const int32_t C = a.map_chunk, R = a.P * a.Rp;
+    // one template per (row width, dim order, box height); the kinds that share one
+    // (hit and miss plane rows) share it
+    for (int k = 0; k < kMapsPerReq; ++k) {
+        if (!(a.map_ops & map_bit(k)) || k == MAP_MISS || k == MAP_MISS_TAIL) continue;
+        const int width = kind_token_rows(k) ? 1 : 0, height = kind_tail(k) ? 1 : 0;
+        const int32_t rows = kind_rows(k, a.B, a.P, a.Rp);
+        for (int order = 0; order < 2; ++order) {
+            if (encode_template(&a.tmpl[width][order][height], d_plan, C, R, width ? R : a.Rp,
+                                rows, order != 0))
+                continue;
+            a.map_ops &= ~map_bit(k);  // and the miss kind that shares the template
+            if (k == MAP_HIT) a.map_ops &= ~map_bit(MAP_MISS);
+            if (k == MAP_HIT_TAIL) a.map_ops &= ~map_bit(MAP_MISS_TAIL);
+        }
     }
     return a;
 }

@@ -87,7 +87,7 @@ def test_plan_layout_is_consistent(lib):
         assert all(o % 256 == 0 for o in off)
         need = {1: 8 * (n + 1), 2: 8 * (n + 1), 3: 8 * (n + 1), 4: 4 * N, 5: 4 * N,
                 6: 128 * N, 7: 8 * 4 * L, 8: 4 * ((N + 31) // 32),
-                10: (3 * 128 + 4) * n + 128}  # tensor maps (128-byte aligned), map flags
+                10: (6 * 128 + 4) * n + 128}  # tensor maps (128-byte aligned), map flags
         starts = sorted((off[k], k) for k in need)
         ends = [s for s, _ in starts[1:]] + [off[9]]
         assert starts[0][0] >= 256

@@ -161,6 +161,31 @@ def test_random_ragged_batches_through_tensor_maps(case):
     run_parity(spec)
 
 
+TAIL_CASES = {
+    # blocks whose rows do not divide into whole segments, so each block ends in a tail
+    # read through the tail maps: 64-token blocks of 1,152-byte rows (28 + 28 + 8),
+    # 3 KiB planes in 16-token blocks (10 + 6; slice rows of 6 KiB: 5 + 5 + 5 + 1),
+    # 16 KiB planes in 3-token blocks (2 + 1)
+    "latent_rows": dict(L=2, P=1, B=64, Rp=1152, t_hit=[1700, 900, 2500],
+                        t_miss=[130, 2000, 7]),
+    "3k_planes": dict(L=3, P=2, B=16, Rp=3072, t_hit=[600, 37], t_miss=[450, 200],
+                      source="permuted"),
+    "16k_planes": dict(L=2, P=2, B=3, Rp=16384, t_hit=[40, 25], t_miss=[17, 40],
+                       miss_order="token"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(TAIL_CASES))
+def test_block_tails_through_tensor_maps(name):
+    spec = workloads.custom_spec(name, **TAIL_CASES[name], table="perm", seed=61)
+    hb = host_buffers(spec)
+    gb, _ = device_batch(spec, hb)
+    gb.plan()
+    flags = gb.d_plan.cpu().numpy()[256:256 + 128 * gb.n_items].view(np.int32).reshape(-1, 32)[:, 29]
+    assert (flags & (1 << 3)).any(), "no block-tail maps of the hit rows were built"
+    run_parity(spec)
+
+
 SCALED = {
     # the shapes of the four larger workloads, with fewer layers and tokens
     "llama3_8b_agentic": dict(L=3, P=2, B=16, Rp=2048, t_hit=[3000], t_miss=[77], table="perm"),

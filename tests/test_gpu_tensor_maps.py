@@ -1,8 +1,9 @@
 """The plan's tensor maps, checked without running a single tensor load.
 
-kvl_batch_plan builds, on the device, a tensor map for each strided row source of a
+kvl_batch_plan builds, on the device, tensor maps for each strided row source of a
 request (hit rows read a plane at a time, hit rows read a whole token row at a time
-for the slice, miss rows), by editing a host-encoded template with
+for the slice, miss rows; each with a box of a whole segment's rows and one of a
+block's tail), by editing a host-encoded template with
 `tensormap.replace`.  Here every map the plan wrote is compared, byte for byte, with
 the map the driver's own host encoder (cuTensorMapEncodeTiled) makes for the view
 that the request's strides declare, and every item record's map flags and
@@ -34,8 +35,10 @@ pytestmark = pytest.mark.gpu
 STAGE = 32 * 1024
 MAX_STRIDE = 1 << 40
 MIN_SPAN = 1 << 20
-MAP_HIT, MAP_SLICE, MAP_MISS = 0, 1, 2
-F_HIT, F_SLICE, F_MISS, F_HIT_LAYER_FIRST, F_MISS_LAYER_FIRST = 1, 2, 4, 8, 16
+MAP_HIT, MAP_SLICE, MAP_MISS, MAP_HIT_TAIL, MAP_SLICE_TAIL, MAP_MISS_TAIL = range(6)
+KINDS = 6          # maps per request
+TAIL = 3           # a kind's block-tail kind is kind + TAIL
+F_HIT_LAYER_FIRST, F_MISS_LAYER_FIRST = 64, 128   # record flags beside bit `kind`
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -58,13 +61,23 @@ def seg_rows(B, w):
     return min(B, STAGE // w)
 
 
+def kind_width(kind, P, Rp):
+    return P * Rp if kind in (MAP_SLICE, MAP_SLICE_TAIL) else Rp
+
+
+def kind_rows(kind, B, P, Rp):
+    """Box rows: a whole segment, or a block's tail (B mod the segment rows)."""
+    m = seg_rows(B, kind_width(kind, P, Rp))
+    return m if kind < TAIL else (B % m if m else 0)
+
+
 def map_ops(P, B, Rp):
     C, R = chunk_bytes(Rp), P * Rp
     ops = 0
-    if C and Rp // C <= 256 and seg_rows(B, Rp) <= 256:
-        ops |= F_HIT | F_MISS
-    if C and R <= STAGE and R // C <= 256 and seg_rows(B, R) <= 256:
-        ops |= F_SLICE
+    for k in range(KINDS):
+        w = kind_width(k, P, Rp)
+        if C and w <= STAGE and w // C <= 256 and 1 <= kind_rows(k, B, P, Rp) <= 256:
+            ops |= 1 << k
     return ops
 
 
@@ -113,20 +126,20 @@ def expected_maps(q, L, P, B, Rp):
             n_tok, n_blk = t_hit, 1
         if n_tok:
             args = (int(q["hit_src"]), n_tok, ts, L, int(q["hit_layer_stride"]), n_blk, bs, R, C)
-            v = view(*args, Rp, seg_rows(B, Rp)) if ops & F_HIT else None
+            for k in (MAP_HIT, MAP_SLICE, MAP_HIT_TAIL, MAP_SLICE_TAIL):
+                v = view(*args, kind_width(k, P, Rp), kind_rows(k, B, P, Rp)) \
+                    if ops & (1 << k) else None
+                if v:
+                    out[k] = v
+                    flags |= (1 << k) | (F_HIT_LAYER_FIRST if v[3] else 0)
+    if t_miss > 0:
+        for k in (MAP_MISS, MAP_MISS_TAIL):
+            v = view(int(q["miss_src"]), t_miss, int(q["miss_token_stride"]), L,
+                     int(q["miss_layer_stride"]), 1, 0, R, C, Rp, kind_rows(k, B, P, Rp)) \
+                if ops & (1 << k) else None
             if v:
-                out[MAP_HIT] = v
-                flags |= F_HIT | (F_HIT_LAYER_FIRST if v[3] else 0)
-            v = view(*args, R, seg_rows(B, R)) if ops & F_SLICE else None
-            if v and (MAP_HIT not in out or v[3] == out[MAP_HIT][3]):
-                out[MAP_SLICE] = v
-                flags |= F_SLICE | (F_HIT_LAYER_FIRST if v[3] else 0)
-    if ops & F_MISS and t_miss > 0:
-        v = view(int(q["miss_src"]), t_miss, int(q["miss_token_stride"]), L,
-                 int(q["miss_layer_stride"]), 1, 0, R, C, Rp, seg_rows(B, Rp))
-        if v:
-            out[MAP_MISS] = v
-            flags |= F_MISS | (F_MISS_LAYER_FIRST if v[3] else 0)
+                out[k] = v
+                flags |= (1 << k) | (F_MISS_LAYER_FIRST if v[3] else 0)
     return out, flags
 
 
@@ -169,10 +182,10 @@ def check_plan(g, n_req, reqs, d_reqs, tables, src_tables, d_plan, layout):
         want, flags = expected_maps(q, L, P, B, Rp)
         flags_of.append(flags)
         for kind, (dims, strides, box, _) in want.items():
-            at = maps_at + (r * 3 + kind) * 128
+            at = maps_at + (r * KINDS + kind) * 128
             got = plan[at:at + 128]
-            exp = host_encode(int(q["hit_src"] if kind != MAP_MISS else q["miss_src"]),
-                              dims, strides, box)
+            miss = kind in (MAP_MISS, MAP_MISS_TAIL)
+            exp = host_encode(int(q["miss_src"] if miss else q["hit_src"]), dims, strides, box)
             assert np.array_equal(got, exp), (r, kind, dims, strides, box,
                                               np.nonzero(got != exp)[0])
             n_maps += 1
@@ -291,7 +304,8 @@ def test_plan_maps_equal_the_host_encoder(case):
 
 
 def test_synthetic_cases_cover_every_map_kind_and_order():
-    """The random cases above build maps of each kind in both dim orders."""
+    """The random cases above build maps of each kind, the whole-segment kinds in
+    both dim orders."""
     seen = set()
     for case in range(CASES):
         geo, reqs, _, _, _ = synthetic_case(4100 + case)
@@ -299,12 +313,13 @@ def test_synthetic_cases_cover_every_map_kind_and_order():
             want, _ = expected_maps(q, geo.n_layers, geo.n_planes, geo.block_tokens,
                                     geo.plane_row_bytes)
             seen |= {(k, v[3]) for k, v in want.items()}
-    assert seen == {(k, o) for k in (MAP_HIT, MAP_SLICE, MAP_MISS) for o in (False, True)}
+    assert {k for k, _ in seen} == set(range(KINDS))
+    assert {(k, o) for k in (MAP_HIT, MAP_SLICE, MAP_MISS) for o in (False, True)} <= seen
 
 
 def test_workload_shapes_get_maps():
     """Requests shaped like the benchmark's workloads, over real buffers, each get
-    their three maps."""
+    all their maps."""
     for name, kw in {
         "llama3_8b_agentic": dict(L=32, P=2, B=16, Rp=2048, t_hit=[3000], t_miss=[77]),
         "qwen3_32b_long": dict(L=8, P=2, B=64, Rp=2048, t_hit=[1280], t_miss=[300],
@@ -325,7 +340,10 @@ def test_workload_shapes_get_maps():
                 nsrc = -(-lq.t_hit // spec.B)
                 src[r] = hb.src_tables[lq.src_table_off:lq.src_table_off + nsrc]
         n = check_plan(gb.g, gb.n_req, reqs, gb.d_reqs, hb.tables, src, gb.d_plan, gb.layout)
-        assert n == 3 * spec.n_req, name
+        # three kinds per request, and the three block-tail kinds where blocks have a
+        # tail (the latent batch's 64-token blocks of 1,152-byte rows: 28 + 28 + 8)
+        tails = sum(kind_rows(k, spec.B, spec.P, spec.Rp) > 0 for k in range(TAIL, KINDS))
+        assert n == (3 + tails) * spec.n_req, name
 
 
 def test_small_or_overlapping_sources_get_no_map():
