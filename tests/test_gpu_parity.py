@@ -252,16 +252,27 @@ def test_block_major_object_files():
     run_parity(spec)
 
 
+MULTI_LAYER_SPECS = {
+    # sources far below a tensor map's span (every row its own load), and sources of
+    # megabytes (whole segments through the maps, each unit at its own layer)
+    "small_rows": dict(L=4, P=2, B=16, Rp=256, t_hit=[300, 0, 77, 41], t_miss=[20, 33, 0, 5]),
+    "mapped_rows": dict(L=4, P=2, B=16, Rp=2048, t_hit=[700, 0, 300, 41],
+                        t_miss=[400, 33, 0, 5]),
+}
+
+
+@pytest.mark.parametrize("rows", sorted(MULTI_LAYER_SPECS))
 @pytest.mark.parametrize("layers", [(0, 4), (1, 2), (3, 1)])
-def test_multi_layer_launches_equal_the_layer_by_layer_oracle(layers):
+def test_multi_layer_launches_equal_the_layer_by_layer_oracle(layers, rows):
     first, count = layers
-    spec = workloads.custom_spec(L=4, P=2, B=16, Rp=256, t_hit=[300, 0, 77, 41],
-                                 t_miss=[20, 33, 0, 5], source="permuted", seed=91,
+    spec = workloads.custom_spec(rows, **MULTI_LAYER_SPECS[rows], source="permuted", seed=91,
                                  objects="block")
     hb = host_buffers(spec)
     gb, d = device_batch(spec, hb)
     ob = oracle_batch(spec, hb)
     gb.plan()
+    flags = gb.d_plan.cpu().numpy()[256:256 + 128 * gb.n_items].view(np.int32).reshape(-1, 32)[:, 29]
+    assert bool((flags & 1).any()) == (rows == "mapped_rows")
     R = spec.R
     n_hit, n_tok = ob.total_hit() * R, ob.total_tokens() * R
     hit_out = sentinel_dev(count * n_hit)
