@@ -634,11 +634,9 @@ def run_gpu(args):
     peak, peak_kind = hbm_peak()
     achieved = per_op[dom]["gbs"]
     # the pipeline depth most of the dominant op's launches ran with (the kernels are
-    # instantiated per depth: 3 stages when sharing SMs with a neighbour launch or, alone,
-    # for rows under 2 KiB (two CTAs per SM); else 6)
+    # instantiated per depth: 3 stages when sharing SMs with a neighbour launch, else 6)
     shares = launch_flags(dom, 1, groups[1][0]) if len(groups) > 1 else 0
-    short_rows = (dom == "slice" and spec.R < 2048) or (dom == "merge_scatter" and spec.Rp < 2048)
-    kname = f"{KERNEL_NAMES[dom]}<{3 if shares or short_rows else 6}>"
+    kname = f"{KERNEL_NAMES[dom]}<{3 if shares else 6}>"
     traffic = recorded_traffic(kname, spec.name) if K == 1 else None
     roofline = {"bound": "hbm", "kernel": kname + f" ({dom})",
                 "achieved": achieved, "peak": peak, "unit": "GB/s",

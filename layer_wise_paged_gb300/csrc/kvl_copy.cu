@@ -759,11 +759,10 @@ constexpr void (*kernel_of())(CopyArgs)
     }
 }
 
-// Grid: per_sm CTAs on every SM (or the caller's cap); opts each kernel into its
-// shared memory once per device (concurrent first calls may both set the same
-// attribute).
+// Grid: one CTA on every SM (or the caller's cap); opts each kernel into its shared
+// memory once per device (concurrent first calls may both set the same attribute).
 template <int OP, int HOST, int STAGES>
-int grid_size(const kvl_launch *opts, int per_sm)
+int grid_size(const kvl_launch *opts)
 {
     static std::atomic<bool> ready[kMaxDevices];
     int dev = 0;
@@ -775,16 +774,16 @@ int grid_size(const kvl_launch *opts, int per_sm)
             return 0;
         ready[dev].store(true, std::memory_order_release);
     }
-    const int full = sm_count() * per_sm;
+    const int full = sm_count();
     if (opts && opts->max_ctas > 0 && opts->max_ctas < full) return opts->max_ctas;
     return full;
 }
 
 template <int OP, int HOST, int STAGES>
-kvl_status launch_mode(const CopyArgs &a, const kvl_launch *opts, void *stream, int per_sm = 1)
+kvl_status launch_mode(const CopyArgs &a, const kvl_launch *opts, void *stream)
 {
     constexpr int kSmemBytes = STAGES * kStageBytes;
-    const int grid = grid_size<OP, HOST, STAGES>(opts, per_sm);
+    const int grid = grid_size<OP, HOST, STAGES>(opts);
     if (grid <= 0) return KVL_ECUDA;
 #if KVL_PDL
     cudaLaunchConfig_t cfg = {};
@@ -815,13 +814,6 @@ kvl_status launch(const CopyArgs &args, const kvl_launch *opts, void *stream)
     if (host == KVL_LAUNCH_HOST_DST) return launch_mode<OP, 2, kDeepStages>(a, opts, stream);
     if (a.flags & (KVL_LAUNCH_OVERLAP_PREVIOUS | KVL_LAUNCH_SHARE_SMS))
         return launch_mode<OP, 0, kShallowStages>(a, opts, stream);
-    // A launch alone on the whole GPU whose source rows are short (slice and
-    // merge-scatter rows under 2 KiB, one bulk copy each) runs two 96 KiB CTAs per SM:
-    // one warp issues rows too slowly to hold the SM's share of the bandwidth, two
-    // warps do.  Longer rows and contiguous segments keep one 192 KiB CTA per SM.
-    const int row_bytes = OP == OP_SLICE ? a.P * a.Rp : a.Rp;
-    if ((OP == OP_SLICE || OP == OP_MERGE) && row_bytes < 2048 && !(opts && opts->max_ctas > 0))
-        return launch_mode<OP, 0, kShallowStages>(a, opts, stream, 2);
     return launch_mode<OP, 0, kDeepStages>(a, opts, stream);
 }
 
