@@ -161,6 +161,36 @@ def test_random_ragged_batches_through_tensor_maps(case):
     run_parity(spec)
 
 
+def _mapped_spec(seed):
+    """A random batch whose sources span a megabyte or more (tensor maps), over plane
+    rows whose segments leave block tails (1,152, 1,536, 3,072 B ...), odd block
+    sizes, permuted or contiguous sources, both miss layouts, empty hit prefixes."""
+    g = np.random.default_rng(seed)
+    P = int(g.integers(1, 3))
+    Rp = int(g.choice([256, 1152, 1536, 2048, 3072, 4096, 8192]))
+    if P * Rp > 32768:
+        P = 1
+    B = int(g.choice([3, 7, 16, 31, 64]))
+    L = int(g.integers(2, 6))
+    n = int(g.choice([1, 2, 4, 7]))
+    lo = -(-(1 << 20) // ((L - 1) * P * Rp)) + 1
+    t_hit = g.integers(lo // 2, 3 * lo, n)
+    t_miss = g.integers(0, 2 * lo, n)
+    if g.random() < 0.3:
+        t_hit[0] = 0
+    return g, workloads.custom_spec(
+        f"mapped{seed}", L=L, P=P, B=B, Rp=Rp, t_hit=t_hit, t_miss=t_miss,
+        table=str(g.choice(["perm", "fragmented"])),
+        source=str(g.choice(["contiguous", "permuted"])),
+        miss_order=str(g.choice(["layer", "token"])), seed=seed,
+        objects=str(g.choice(["layer", "block"])))
+
+
+@pytest.mark.parametrize("case", range(40))
+def test_random_mapped_batches_with_tails(case):
+    run_parity(_mapped_spec(96000 + case)[1])
+
+
 TAIL_CASES = {
     # blocks whose rows do not divide into whole segments, so each block ends in a tail
     # read through the tail maps: 64-token blocks of 1,152-byte rows (28 + 28 + 8),
@@ -447,22 +477,27 @@ def test_gather_writes_host_objects_and_scatter_back_reads_them():
     assert gb.status() == (0, 0)
 
 
-@pytest.mark.parametrize("case", range(30))
+@pytest.mark.parametrize("case", range(46))
 def test_random_launch_plans_equal_the_oracle(case):
     """Random ragged batches under random launch plans: per op, random layers per
     launch, SM budgets and overlap flags (every launch of a phase after the first may
     overlap its predecessor; the first shares SMs or not).  Budgets as small as one
-    CTA let long chains of launches run at once."""
+    CTA let long chains of launches run at once.  Cases 30 and up draw batches large
+    enough for tensor maps."""
     import layer_wise_paged_gb300 as kvl
-    g = np.random.default_rng(7100 + case)
-    L = int(g.integers(2, 7))
-    n = int(g.choice([1, 3, 9]))
-    spec = workloads.custom_spec(
-        L=L, P=int(g.integers(1, 3)), B=int(g.choice([4, 16, 64])),
-        Rp=int(g.choice([64, 1152, 2048])), t_hit=g.integers(0, 900, n),
-        t_miss=g.integers(0, 300, n), table=str(g.choice(["perm", "fragmented"])),
-        source=str(g.choice(["contiguous", "permuted"])), seed=7200 + case,
-        objects=str(g.choice(["layer", "block"])))
+    if case >= 30:
+        g, spec = _mapped_spec(97000 + case)
+        L = spec.L
+    else:
+        g = np.random.default_rng(7100 + case)
+        L = int(g.integers(2, 7))
+        n = int(g.choice([1, 3, 9]))
+        spec = workloads.custom_spec(
+            L=L, P=int(g.integers(1, 3)), B=int(g.choice([4, 16, 64])),
+            Rp=int(g.choice([64, 1152, 2048])), t_hit=g.integers(0, 900, n),
+            t_miss=g.integers(0, 300, n), table=str(g.choice(["perm", "fragmented"])),
+            source=str(g.choice(["contiguous", "permuted"])), seed=7200 + case,
+            objects=str(g.choice(["layer", "block"])))
     hb = host_buffers(spec)
     gb, d = device_batch(spec, hb)
     ob = oracle_batch(spec, hb)
