@@ -193,14 +193,19 @@ void kvl_plan_layout(const kvl_geom *geom, int32_t n_req, size_t off[11]);
  * full-block id of a hit block (in [0, hit_src_blocks)) and, if check_injective,
  * that no pool block id repeats.
  * The plan also describes each request's strided row sources (hit rows, miss rows)
- * by tensor maps, built on the device from a template, when their strides lay the
- * rows out without overlap (each stride at least the extent below it); the copy
+ * by tensor maps, built on the device from templates that the host encodes with the
+ * driver's cuTensorMapEncodeTiled (looked up through the runtime on the first plan
+ * call; host work only, nothing allocated), when their strides lay the rows out
+ * without overlap (each stride at least the extent below it) and some dimension spans
+ * at least 1 MiB; the copy
  * calls then read a segment of rows of one source (a whole segment, or the rows a
  * block has left after its whole segments) with one tiled bulk-tensor load instead
  * of one bulk load per row.  The maps span exactly the rows a request
  * declares: T_hit rows of a full block without a table, all B token rows of each
  * of the hit_src_blocks blocks with a table (so with a table every one of those
  * blocks must be whole), and T_miss rows of the miss KV, each over all L layers.
+ * Sources without maps (or a driver without the encoder) are read one bulk load per
+ * row: the results are the same bytes either way.
  *   geom            host pointer
  *   d_reqs          device array of n_req requests (caller-owned, read only; may be
  *                   NULL when n_req == 0)
