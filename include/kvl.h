@@ -237,15 +237,22 @@ kvl_status kvl_batch_plan(const kvl_geom *geom, int32_t n_req, const kvl_request
  * kvl_plan_layout(...)[8] bytes (everything before the bitmap section); the plan it
  * writes is the same as kvl_batch_plan's and the copy calls accept it.
  * It allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
- * The first call on a device looks up the array's device address (once per device,
- * with that device current) and caches it; make that first call before any stream
- * capture.
+ * The array's device address belongs to the CUDA context the library's module was
+ * loaded into.  Every call that is not being captured into a graph looks it up again
+ * (cudaGetSymbolAddress, with the device current) and remembers it with the current
+ * context's id; a call made while `stream` is capturing uses that remembered address
+ * only if the current context is the one it was taken in, and otherwise returns
+ * KVL_ECUDA with nothing launched.  So make one call on the device, outside capture,
+ * before capturing one, and again after a cudaDeviceReset or a context switch.
  * Limits and sharing: pool_blocks above KVL_STATIC_SCRATCH_POOL_BLOCKS returns
  * KVL_EINVAL and launches nothing.  Every call on a device shares the one array,
  * which keeps the last call's contents; each call clears the bits it uses before
- * using them, but calls that overlap on the GPU (other streams, other host threads)
- * race on the array and may report duplicates wrongly.  Other arguments, checks and
- * status codes are those of kvl_batch_plan. */
+ * using them.  Calls that overlap on the GPU (other streams, other host threads)
+ * race on the array in both directions: one call's bits can make another report a
+ * duplicate that is not there, and one call's clearing can erase another's bits, so
+ * a real duplicate can pass with KVL_OK and the copy calls would then give one pool
+ * block two writers.  Serialise such calls.  Other arguments, checks and status
+ * codes are those of kvl_batch_plan. */
 #define KVL_STATIC_SCRATCH_POOL_BLOCKS (1 << 22)
 kvl_status kvl_batch_plan_static_scratch(const kvl_geom *geom, int32_t n_req,
                                          const kvl_request *d_reqs, const int32_t *d_block_tables,
@@ -260,12 +267,15 @@ kvl_status kvl_batch_plan_static_scratch(const kvl_geom *geom, int32_t n_req,
  * layer >= 0, layer_count >= 1, layer + layer_count <= L, pool_blocks * layer_count
  * < 2^31; otherwise KVL_EINVAL.  `launch` may be NULL (the whole GPU, no flags); a
  * negative max_ctas, an unknown flag or both host flags together is KVL_EINVAL.
- * d_plan is a plan built for this geom: a device buffer of at least
- * kvl_plan_layout(geom, 0)[8] bytes (true of any plan kvl_batch_plan accepted for it).
- * The kernels read its item records before they check the header, so a buffer
- * sized for a smaller pool may be read past its end; a plan built for other arrays or
- * another geometry (L, P, B, Rp or N) that is large enough is refused (KVL_EINVAL in
- * its status).
+ * d_plan is a plan built for this geom, and plan_bytes the size of the buffer at d_plan
+ * (the plan_bytes the plan was built with, or the bytes a static-scratch plan needs).
+ * plan_bytes below kvl_plan_layout(geom, 0)[8], the smallest plan of this geometry,
+ * returns KVL_EINVAL and launches nothing, so no kernel reads past a buffer the host
+ * knows to be too small.  The kernels read nothing of the plan beyond plan_bytes: a
+ * plan whose recorded request count needs more than plan_bytes (a buffer sized for
+ * fewer requests than the plan in it holds), or that was built for other arrays or
+ * another geometry (L, P, B, Rp or N), is refused on the device (KVL_EINVAL in its
+ * status) before any of its n_req-sized sections is read.
  * d_reqs and d_block_tables are the arrays the plan was built from; NULL only if it was
  * built from NULL (a batch of no requests); other NULLs are refused on the device. */
 
@@ -274,9 +284,9 @@ kvl_status kvl_batch_plan_static_scratch(const kvl_geom *geom, int32_t n_req,
  * of pe_read_path / de_read_path).  Writes, for each layer of the launch, sum(T_hit)
  * rows of R bytes to d_hit_out (device, caller-owned): launch layer i (= l - layer) at
  * row i*sum(T_hit) + hit_off[r] + t. */
-kvl_status kvl_slice_layer(const kvl_geom *geom, const void *d_plan, const kvl_request *d_reqs,
-                           int32_t layer, int32_t layer_count, void *d_hit_out,
-                           const kvl_launch *launch, void *stream);
+kvl_status kvl_slice_layer(const kvl_geom *geom, const void *d_plan, size_t plan_bytes,
+                           const kvl_request *d_reqs, int32_t layer, int32_t layer_count,
+                           void *d_hit_out, const kvl_launch *launch, void *stream);
 
 /* kvl_merge_scatter_paged -- slice, concatenate and scatter in one pass:
  * complete_layer[l] = hit_layer[l] rows then miss_layer[l] rows (DualPath KV Loading,
@@ -286,7 +296,7 @@ kvl_status kvl_slice_layer(const kvl_geom *geom, const void *d_plan, const kvl_r
  *                   launch's layers named by the tables are written
  *   d_complete_out  NULL, or device memory that also receives complete_layer[l]:
  *                   launch layer i at row i*sum(T_all) + tok_off[r] + t, R bytes each */
-kvl_status kvl_merge_scatter_paged(const kvl_geom *geom, const void *d_plan,
+kvl_status kvl_merge_scatter_paged(const kvl_geom *geom, const void *d_plan, size_t plan_bytes,
                                    const kvl_request *d_reqs, const int32_t *d_block_tables,
                                    int32_t layer, int32_t layer_count, void *d_pool,
                                    void *d_complete_out, const kvl_launch *launch, void *stream);
@@ -297,7 +307,7 @@ kvl_status kvl_merge_scatter_paged(const kvl_geom *geom, const void *d_plan,
  * 阅读笔记, 前置知识 5 eq. (4); the worked trace's 8,000 per-layer entries for 4,000
  * blocks).  direction KVL_SCATTER_BACK: the inverse, restoring objects into their
  * paged blocks (伪代码 1 retrieve_layer).  Each request's `objects` must be non-NULL. */
-kvl_status kvl_gather_layer_objects(const kvl_geom *geom, const void *d_plan,
+kvl_status kvl_gather_layer_objects(const kvl_geom *geom, const void *d_plan, size_t plan_bytes,
                                     const kvl_request *d_reqs, const int32_t *d_block_tables,
                                     int32_t layer, int32_t layer_count, void *d_pool,
                                     int32_t direction, const kvl_launch *launch, void *stream);

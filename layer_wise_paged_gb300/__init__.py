@@ -72,9 +72,9 @@ def lib():
         L.kvl_batch_plan.argtypes = [gp, i32, vp, vp, i32, vp, sz, vp]
         L.kvl_batch_plan_static_scratch.argtypes = [gp, i32, vp, vp, i32, vp, sz, vp]
         lp = ctypes.POINTER(kvl_launch)
-        L.kvl_slice_layer.argtypes = [gp, vp, vp, i32, i32, vp, lp, vp]
-        L.kvl_merge_scatter_paged.argtypes = [gp, vp, vp, vp, i32, i32, vp, vp, lp, vp]
-        L.kvl_gather_layer_objects.argtypes = [gp, vp, vp, vp, i32, i32, vp, i32, lp, vp]
+        L.kvl_slice_layer.argtypes = [gp, vp, sz, vp, i32, i32, vp, lp, vp]
+        L.kvl_merge_scatter_paged.argtypes = [gp, vp, sz, vp, vp, i32, i32, vp, vp, lp, vp]
+        L.kvl_gather_layer_objects.argtypes = [gp, vp, sz, vp, vp, i32, i32, vp, i32, lp, vp]
         L.kvl_read_status.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i64), vp]
         L.kvl_diag_wait_timeout.argtypes, L.kvl_diag_wait_timeout.restype = [i32, vp, vp], i32
         L.kvl_status_string.argtypes, L.kvl_status_string.restype = [i32], ctypes.c_char_p
@@ -138,24 +138,27 @@ def kvl_batch_plan_static_scratch(g, n_req, d_reqs, d_block_tables, check_inject
 KVL_STATIC_SCRATCH_POOL_BLOCKS = 1 << 22
 
 
-def kvl_slice_layer(g, d_plan, d_reqs, layer, layer_count, d_hit_out, max_ctas=None,
-                    stream=None) -> int:
-    return int(lib().kvl_slice_layer(_g(g), _p(d_plan), _p(d_reqs), int(layer), int(layer_count),
-                                     _p(d_hit_out), _launch(max_ctas), _p(stream)))
+def kvl_slice_layer(g, d_plan, plan_bytes, d_reqs, layer, layer_count, d_hit_out,
+                    max_ctas=None, stream=None) -> int:
+    return int(lib().kvl_slice_layer(_g(g), _p(d_plan), int(plan_bytes), _p(d_reqs), int(layer),
+                                     int(layer_count), _p(d_hit_out), _launch(max_ctas),
+                                     _p(stream)))
 
 
-def kvl_merge_scatter_paged(g, d_plan, d_reqs, d_block_tables, layer, layer_count, d_pool,
-                            d_complete_out=None, max_ctas=None, stream=None) -> int:
-    return int(lib().kvl_merge_scatter_paged(_g(g), _p(d_plan), _p(d_reqs), _p(d_block_tables),
-                                             int(layer), int(layer_count), _p(d_pool),
-                                             _p(d_complete_out), _launch(max_ctas), _p(stream)))
+def kvl_merge_scatter_paged(g, d_plan, plan_bytes, d_reqs, d_block_tables, layer, layer_count,
+                            d_pool, d_complete_out=None, max_ctas=None, stream=None) -> int:
+    return int(lib().kvl_merge_scatter_paged(_g(g), _p(d_plan), int(plan_bytes), _p(d_reqs),
+                                             _p(d_block_tables), int(layer), int(layer_count),
+                                             _p(d_pool), _p(d_complete_out), _launch(max_ctas),
+                                             _p(stream)))
 
 
-def kvl_gather_layer_objects(g, d_plan, d_reqs, d_block_tables, layer, layer_count, d_pool,
-                             direction, max_ctas=None, stream=None) -> int:
-    return int(lib().kvl_gather_layer_objects(_g(g), _p(d_plan), _p(d_reqs), _p(d_block_tables),
-                                              int(layer), int(layer_count), _p(d_pool),
-                                              int(direction), _launch(max_ctas), _p(stream)))
+def kvl_gather_layer_objects(g, d_plan, plan_bytes, d_reqs, d_block_tables, layer, layer_count,
+                             d_pool, direction, max_ctas=None, stream=None) -> int:
+    return int(lib().kvl_gather_layer_objects(_g(g), _p(d_plan), int(plan_bytes), _p(d_reqs),
+                                              _p(d_block_tables), int(layer), int(layer_count),
+                                              _p(d_pool), int(direction), _launch(max_ctas),
+                                              _p(stream)))
 
 
 def kvl_read_status(d_plan, stream=None):

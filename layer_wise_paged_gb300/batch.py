@@ -112,26 +112,29 @@ class Batch:
                              _stream(stream)), "kvl_batch_plan")
 
     def slice_layer(self, layer, hit_out, stream=None, layer_count=1, max_ctas=None, flags=0):
-        check(kvl_slice_layer(self.g, _ptr(self.d_plan), _ptr(self.d_reqs), layer, layer_count,
-                              _ptr(hit_out), self._opts(max_ctas, flags), _stream(stream)),
-              "kvl_slice_layer")
+        check(kvl_slice_layer(self.g, _ptr(self.d_plan), self.plan_bytes, _ptr(self.d_reqs),
+                              layer, layer_count, _ptr(hit_out), self._opts(max_ctas, flags),
+                              _stream(stream)), "kvl_slice_layer")
 
     def merge_scatter(self, layer, pool, complete_out=None, stream=None, layer_count=1,
                       max_ctas=None, flags=0):
-        check(kvl_merge_scatter_paged(self.g, _ptr(self.d_plan), _ptr(self.d_reqs),
-                                      _ptr(self.tables), layer, layer_count, _ptr(pool),
+        check(kvl_merge_scatter_paged(self.g, _ptr(self.d_plan), self.plan_bytes,
+                                      _ptr(self.d_reqs), _ptr(self.tables), layer, layer_count,
+                                      _ptr(pool),
                                       _ptr(complete_out), self._opts(max_ctas, flags),
                                       _stream(stream)), "kvl_merge_scatter_paged")
 
     def gather(self, layer, pool, stream=None, layer_count=1, max_ctas=None, flags=0):
-        check(kvl_gather_layer_objects(self.g, _ptr(self.d_plan), _ptr(self.d_reqs),
-                                       _ptr(self.tables), layer, layer_count, _ptr(pool),
+        check(kvl_gather_layer_objects(self.g, _ptr(self.d_plan), self.plan_bytes,
+                                       _ptr(self.d_reqs), _ptr(self.tables), layer, layer_count,
+                                       _ptr(pool),
                                        KVL_GATHER, self._opts(max_ctas, flags), _stream(stream)),
               "kvl_gather_layer_objects")
 
     def scatter_back(self, layer, pool, stream=None, layer_count=1, max_ctas=None, flags=0):
-        check(kvl_gather_layer_objects(self.g, _ptr(self.d_plan), _ptr(self.d_reqs),
-                                       _ptr(self.tables), layer, layer_count, _ptr(pool),
+        check(kvl_gather_layer_objects(self.g, _ptr(self.d_plan), self.plan_bytes,
+                                       _ptr(self.d_reqs), _ptr(self.tables), layer, layer_count,
+                                       _ptr(pool),
                                        KVL_SCATTER_BACK, self._opts(max_ctas, flags),
                                        _stream(stream)), "kvl_gather_layer_objects")
 

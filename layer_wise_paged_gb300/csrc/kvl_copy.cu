@@ -66,6 +66,7 @@ static_assert(kStageBytes % 16 == 0 && kShallowStages >= 2 && kDeepStages >= kSh
 
 struct CopyArgs {
     void *plan;
+    uint64_t plan_bytes;  // bytes of the caller's plan buffer: no plan read goes beyond
     const kvl_request *reqs;
     const int32_t *tables;
     uint8_t *pool;
@@ -336,15 +337,18 @@ __device__ __forceinline__ T shfl_ptr(T p, int src)
 // ---- plan checks and metadata ------------------------------------------------
 
 // A plan is usable when it was built (magic) for this geometry, request array and
-// block tables, and recorded no error.  The checks keep every later index inside
-// the plan's own arrays and the request array it was sized for.
+// block tables, fits the caller's buffer with the request count it records, and
+// recorded no error.  The checks keep every later index inside the plan's own
+// arrays (all of them below plan_bytes) and the request array it was sized for.
 template <int OP>
 __device__ __forceinline__ bool plan_usable(const CopyArgs &a)
 {
     PlanHeader *h = static_cast<PlanHeader *>(a.plan);
+    const int32_t n_req = h->n_req;
     if (h->magic != kPlanMagic || h->pool_blocks != a.N || h->block_tokens != a.B ||
         h->n_layers != a.L || h->n_planes != a.P || h->plane_row_bytes != a.Rp ||
-        h->reqs != a.reqs || (OP != OP_SLICE && h->tables != a.tables)) {
+        h->reqs != a.reqs || (OP != OP_SLICE && h->tables != a.tables) || n_req < 0 ||
+        plan_layout(n_req, a.N, a.L).off[8] > a.plan_bytes) {
         if (blockIdx.x == 0 && threadIdx.x == 0) record_error(h, KVL_EINVAL, 0);
         return false;
     }
@@ -469,14 +473,15 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
         fence_mbar_init();
     }
     // The item records sit at a fixed offset, so this CTA's first record (item
-    // blockIdx.x, below the plan's capacity of N records) is addressed without the
-    // header.  Its line and the header's are fetched into L2 while the previous kernel
-    // drains, and read together once it has finished.
-    const uint8_t *plan_bytes = static_cast<const uint8_t *>(a.plan);
+    // blockIdx.x, below the plan's capacity of N records, which the host has checked
+    // lie inside plan_bytes) is addressed without the header.  Its line and the
+    // header's are fetched into L2 while the previous kernel drains, and read together
+    // once it has finished.
+    const uint8_t *plan_base = static_cast<const uint8_t *>(a.plan);
     const bool first_in_cap = blockIdx.x < a.N;
     const uint32_t *first_rec = reinterpret_cast<const uint32_t *>(
-        plan_bytes + kRecordsOffset + int64_t(blockIdx.x) * int64_t(sizeof(ItemRec)));
-    if (lane == 0) prefetch_l2(plan_bytes);
+        plan_base + kRecordsOffset + int64_t(blockIdx.x) * int64_t(sizeof(ItemRec)));
+    if (lane == 0) prefetch_l2(plan_base);
     if (lane == 1 && first_in_cap) prefetch_l2(first_rec);
     __syncwarp();
     // Everything this kernel reads may come from the previous kernel on the stream,
@@ -759,20 +764,23 @@ constexpr void (*kernel_of())(CopyArgs)
     }
 }
 
-// Grid: one CTA on every SM (or the caller's cap); opts each kernel into its shared
-// memory once per device (concurrent first calls may both set the same attribute).
+// Grid: one CTA on every SM (or the caller's cap).  Opts each kernel into its shared
+// memory once per context: the attribute belongs to the context, so it is set again
+// when the device's current context has changed (after cudaDeviceReset, say); with no
+// context id to compare, on every call.  Concurrent first calls may both set it.
 template <int OP, int HOST, int STAGES>
 int grid_size(const kvl_launch *opts)
 {
-    static std::atomic<bool> ready[kMaxDevices];
+    static std::atomic<unsigned long long> ready_ctx[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
-    if (!ready[dev].load(std::memory_order_acquire)) {
+    const unsigned long long ctx = current_context_id();
+    if (ctx == 0 || ready_ctx[dev].load(std::memory_order_acquire) != ctx) {
         if (cudaFuncSetAttribute(kernel_of<OP, HOST, STAGES>(),
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  STAGES * kStageBytes) != cudaSuccess)
             return 0;
-        ready[dev].store(true, std::memory_order_release);
+        ready_ctx[dev].store(ctx, std::memory_order_release);
     }
     const int full = sm_count();
     if (opts && opts->max_ctas > 0 && opts->max_ctas < full) return opts->max_ctas;
@@ -817,9 +825,9 @@ kvl_status launch(const CopyArgs &args, const kvl_launch *opts, void *stream)
     return launch_mode<OP, 0, kDeepStages>(a, opts, stream);
 }
 
-kvl_status common_checks(const kvl_geom *g, const void *d_plan, const kvl_request *d_reqs,
-                         int32_t layer, int32_t layer_count, int32_t row_bytes,
-                         const kvl_launch *opts)
+kvl_status common_checks(const kvl_geom *g, const void *d_plan, size_t plan_bytes,
+                         const kvl_request *d_reqs, int32_t layer, int32_t layer_count,
+                         int32_t row_bytes, const kvl_launch *opts)
 {
     const kvl_status s = check_geom(g);
     if (s) return s;
@@ -832,6 +840,10 @@ kvl_status common_checks(const kvl_geom *g, const void *d_plan, const kvl_reques
     // plan's own record of the array it was built from
     if (!d_plan) return KVL_EINVAL;
     if (!aligned16(d_plan) || !aligned16(d_reqs)) return KVL_EALIGN;
+    // the smallest plan of this geometry (header, N item records, work list, claim
+    // counters): every plan read a kernel makes before it has checked the header lies
+    // below it
+    if (plan_bytes < plan_layout(0, g->pool_blocks, g->n_layers).off[8]) return KVL_EINVAL;
     if (layer < 0 || layer_count < 1 || layer >= g->n_layers || layer_count > g->n_layers - layer)
         return KVL_EINVAL;
     if (g->pool_blocks * int64_t(layer_count) >= (int64_t(1) << 31)) return KVL_EINVAL;  // unit ids
@@ -839,11 +851,13 @@ kvl_status common_checks(const kvl_geom *g, const void *d_plan, const kvl_reques
     return KVL_OK;
 }
 
-CopyArgs make_args(const kvl_geom *g, const void *d_plan, const kvl_request *d_reqs,
-                   const int32_t *tables, int32_t layer, int32_t layer_count, void *pool, void *out)
+CopyArgs make_args(const kvl_geom *g, const void *d_plan, size_t plan_bytes,
+                   const kvl_request *d_reqs, const int32_t *tables, int32_t layer,
+                   int32_t layer_count, void *pool, void *out)
 {
     CopyArgs a;
     a.plan = const_cast<void *>(d_plan);
+    a.plan_bytes = plan_bytes;
     a.reqs = d_reqs;
     a.tables = tables;
     a.pool = static_cast<uint8_t *>(pool);
@@ -864,53 +878,53 @@ CopyArgs make_args(const kvl_geom *g, const void *d_plan, const kvl_request *d_r
 
 using namespace kvl;
 
-extern "C" kvl_status kvl_slice_layer(const kvl_geom *geom, const void *d_plan,
+extern "C" kvl_status kvl_slice_layer(const kvl_geom *geom, const void *d_plan, size_t plan_bytes,
                                       const kvl_request *d_reqs, int32_t layer, int32_t layer_count,
                                       void *d_hit_out, const kvl_launch *opts, void *stream)
 {
     const int32_t rb = geom ? geom->n_planes * geom->plane_row_bytes : 0;
-    kvl_status s = common_checks(geom, d_plan, d_reqs, layer, layer_count, rb, opts);
+    kvl_status s = common_checks(geom, d_plan, plan_bytes, d_reqs, layer, layer_count, rb, opts);
     if (s) return s;
     if (!d_hit_out) return KVL_EINVAL;
     if (!aligned16(d_hit_out)) return KVL_EALIGN;
-    return launch<OP_SLICE>(
-        make_args(geom, d_plan, d_reqs, nullptr, layer, layer_count, nullptr, d_hit_out), opts,
-        stream);
+    return launch<OP_SLICE>(make_args(geom, d_plan, plan_bytes, d_reqs, nullptr, layer, layer_count,
+                                      nullptr, d_hit_out),
+                            opts, stream);
 }
 
 extern "C" kvl_status kvl_merge_scatter_paged(const kvl_geom *geom, const void *d_plan,
-                                              const kvl_request *d_reqs,
+                                              size_t plan_bytes, const kvl_request *d_reqs,
                                               const int32_t *d_block_tables, int32_t layer,
                                               int32_t layer_count, void *d_pool,
                                               void *d_complete_out, const kvl_launch *opts,
                                               void *stream)
 {
-    kvl_status s = common_checks(geom, d_plan, d_reqs, layer, layer_count,
+    kvl_status s = common_checks(geom, d_plan, plan_bytes, d_reqs, layer, layer_count,
                                  geom ? geom->plane_row_bytes : 0, opts);
     if (s) return s;
     if (!d_pool) return KVL_EINVAL;  // d_block_tables: as d_reqs
     if ((reinterpret_cast<uintptr_t>(d_block_tables) & 3u) || !aligned16(d_pool) ||
         (d_complete_out && !aligned16(d_complete_out)))
         return KVL_EALIGN;
-    return launch<OP_MERGE>(make_args(geom, d_plan, d_reqs, d_block_tables, layer, layer_count,
-                                      d_pool, d_complete_out),
+    return launch<OP_MERGE>(make_args(geom, d_plan, plan_bytes, d_reqs, d_block_tables, layer,
+                                      layer_count, d_pool, d_complete_out),
                             opts, stream);
 }
 
 extern "C" kvl_status kvl_gather_layer_objects(const kvl_geom *geom, const void *d_plan,
-                                               const kvl_request *d_reqs,
+                                               size_t plan_bytes, const kvl_request *d_reqs,
                                                const int32_t *d_block_tables, int32_t layer,
                                                int32_t layer_count, void *d_pool, int32_t direction,
                                                const kvl_launch *opts, void *stream)
 {
-    kvl_status s = common_checks(geom, d_plan, d_reqs, layer, layer_count,
+    kvl_status s = common_checks(geom, d_plan, plan_bytes, d_reqs, layer, layer_count,
                                  geom ? geom->plane_row_bytes : 0, opts);
     if (s) return s;
     if (!d_pool) return KVL_EINVAL;  // d_block_tables: as d_reqs
     if (direction != KVL_GATHER && direction != KVL_SCATTER_BACK) return KVL_EINVAL;
     if ((reinterpret_cast<uintptr_t>(d_block_tables) & 3u) || !aligned16(d_pool)) return KVL_EALIGN;
-    const CopyArgs a =
-        make_args(geom, d_plan, d_reqs, d_block_tables, layer, layer_count, d_pool, nullptr);
+    const CopyArgs a = make_args(geom, d_plan, plan_bytes, d_reqs, d_block_tables, layer,
+                                 layer_count, d_pool, nullptr);
     return direction == KVL_GATHER ? launch<OP_GATHER>(a, opts, stream)
                                    : launch<OP_SCATTER>(a, opts, stream);
 }

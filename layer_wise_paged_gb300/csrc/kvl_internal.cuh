@@ -4,6 +4,10 @@
 
 #include <atomic>
 #include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "kvl.h"
@@ -249,6 +253,38 @@ inline int sm_count()
         cache[dev].store(n, std::memory_order_relaxed);
     }
     return n;
+}
+
+// The current CUDA context's unique id (cuCtxGetId: ids are not reused within a
+// process), or 0 if the driver cannot tell.  Per-context state the library caches
+// (a module's symbol address, a kernel's shared-memory attribute) is keyed by it, so a
+// new context (after cudaDeviceReset, or another context made current) is noticed.
+// The two driver calls are looked up once through the runtime.
+inline unsigned long long current_context_id()
+{
+    static std::once_flag once;
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
 }
 
 inline kvl_status launch_status()

@@ -646,22 +646,38 @@ namespace {
 static __device__ __align__(256) uint32_t g_plan_bitmap[KVL_STATIC_SCRATCH_POOL_BLOCKS / 32];
 
 // Host code must not pass g_plan_bitmap itself to a kernel: on the host that name
-// is a stand-in, not a device address.  The device address is looked up once per
-// device, with that device current, and cached here.
-uint32_t *g_plan_bitmap_dev[kMaxDevices] = {nullptr};
+// is a stand-in, not a device address.  The device address belongs to the module
+// loaded into one CUDA context, and a new context (after cudaDeviceReset, or another
+// context made current) loads the module again, possibly elsewhere.  So the address
+// is looked up again, with the device current, on every call that is not being
+// captured into a graph, and cached with the unique id of the context it belongs to;
+// a call under capture uses the cache only when that id is the current context's, and
+// otherwise refuses (a lookup is not a stream operation a graph could hold).
+struct BitmapAddress {
+    unsigned long long ctx_id = 0;
+    uint32_t *ptr = nullptr;
+};
+BitmapAddress g_plan_bitmap_dev[kMaxDevices];
 std::mutex g_plan_bitmap_mutex;
 
-kvl_status static_bitmap_address(uint32_t **out)
+kvl_status static_bitmap_address(cudaStream_t stream, uint32_t **out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVL_ECUDA;
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &capture) != cudaSuccess) return KVL_ECUDA;
     std::lock_guard<std::mutex> lock(g_plan_bitmap_mutex);
-    if (g_plan_bitmap_dev[dev] == nullptr) {
+    BitmapAddress &c = g_plan_bitmap_dev[dev];
+    if (capture == cudaStreamCaptureStatusNone) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_plan_bitmap) != cudaSuccess || p == nullptr) return KVL_ECUDA;
-        g_plan_bitmap_dev[dev] = static_cast<uint32_t *>(p);
+        c.ptr = static_cast<uint32_t *>(p);
+        c.ctx_id = current_context_id();
+    } else {
+        const unsigned long long id = current_context_id();
+        if (c.ptr == nullptr || id == 0 || id != c.ctx_id) return KVL_ECUDA;
     }
-    *out = g_plan_bitmap_dev[dev];
+    *out = c.ptr;
     return KVL_OK;
 }
 
@@ -686,7 +702,7 @@ extern "C" kvl_status kvl_batch_plan_static_scratch(const kvl_geom *geom, int32_
     if (plan_bytes < plan_layout(n_req, geom->pool_blocks, geom->n_layers).off[8]) return KVL_EINVAL;
 
     uint32_t *bitmap = nullptr;
-    const kvl_status sa = static_bitmap_address(&bitmap);
+    const kvl_status sa = static_bitmap_address(static_cast<cudaStream_t>(stream), &bitmap);
     if (sa) return sa;
 
     PlanArgs a = plan_args(geom, n_req, d_reqs, d_block_tables, check_injective, d_plan);

@@ -226,13 +226,14 @@ static void run_batch(const char *name, int32_t L, int32_t P, int32_t B, int32_t
     CUDA_OK(cudaMalloc((void **)&d_hit_out, (size_t)L * n_hit * R));
     CUDA_OK(cudaMalloc((void **)&d_complete, (size_t)L * n_all * R));
     for (int l = 0; l < L; l++)
-        KVL_OK_(kvl_slice_layer(&geom, d_plan, d_reqs, l, 1, d_hit_out + (size_t)l * n_hit * R,
+        KVL_OK_(kvl_slice_layer(&geom, d_plan, plan_bytes, d_reqs, l, 1, d_hit_out + (size_t)l * n_hit * R,
                                 l ? &next : &first, s));
     for (int l = 0; l < L; l++)
-        KVL_OK_(kvl_merge_scatter_paged(&geom, d_plan, d_reqs, d_tables, l, 1, d_pool,
+        KVL_OK_(kvl_merge_scatter_paged(&geom, d_plan, plan_bytes, d_reqs, d_tables, l, 1, d_pool,
                                         d_complete + (size_t)l * n_all * R, l ? &next : &first, s));
     for (int l = 0; l < L; l++)
-        KVL_OK_(kvl_gather_layer_objects(&geom, d_plan, d_reqs, d_tables, l, 1, d_pool, KVL_GATHER,
+        KVL_OK_(kvl_gather_layer_objects(&geom, d_plan, plan_bytes, d_reqs, d_tables, l, 1, d_pool,
+                                         KVL_GATHER,
                                          l ? &next : &first, s));
     CUDA_OK(cudaStreamSynchronize(s));
 
@@ -257,7 +258,7 @@ static void run_batch(const char *name, int32_t L, int32_t P, int32_t B, int32_t
     /* scatter back into a blank pool: all layers in one launch */
     memset(pool_h, SENTINEL, pool_n);
     CUDA_OK(cudaMemset(d_pool, SENTINEL, pool_n));
-    KVL_OK_(kvl_gather_layer_objects(&geom, d_plan, d_reqs, d_tables, 0, L, d_pool,
+    KVL_OK_(kvl_gather_layer_objects(&geom, d_plan, plan_bytes, d_reqs, d_tables, 0, L, d_pool,
                                      KVL_SCATTER_BACK, NULL, s));
     for (int l = 0; l < L; l++)
         if (oracle_scatter_back(&og, NREQ, oreq, tables, l, pool_h) != 0) failures++;

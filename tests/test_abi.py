@@ -114,13 +114,35 @@ def test_host_checks_answer_before_any_device_work(lib):
     assert kvl.kvl_batch_plan(good, 1, fake, fake, 1, fake + 8, 1 << 20) == kvl.KVL_EALIGN
     assert kvl.kvl_batch_plan(good, 1, fake, fake, 1, fake, 16) == kvl.KVL_EINVAL
     assert kvl.kvl_batch_plan(good, -1, fake, fake, 1, fake, 1 << 20) == kvl.KVL_EINVAL
-    assert kvl.kvl_merge_scatter_paged(good, fake, fake, fake, 2, 1, fake) == kvl.KVL_EINVAL
-    assert kvl.kvl_merge_scatter_paged(good, fake, fake, fake, 0, 1, fake + 4) == kvl.KVL_EALIGN
-    assert kvl.kvl_merge_scatter_paged(good, fake, fake, fake, 0, 0, fake) == kvl.KVL_EINVAL
-    assert kvl.kvl_merge_scatter_paged(good, fake, fake, fake, 1, 2, fake) == kvl.KVL_EINVAL
-    assert kvl.kvl_gather_layer_objects(good, fake, fake, fake, 0, 1, fake, 7) == kvl.KVL_EINVAL
-    assert kvl.kvl_slice_layer(good, fake, fake, 0, 1, 0) == kvl.KVL_EINVAL
+    pb = kvl.kvl_plan_bytes(good, 1)
+    assert kvl.kvl_merge_scatter_paged(good, fake, pb, fake, fake, 2, 1, fake) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(good, fake, pb, fake, fake, 0, 1, fake + 4) == kvl.KVL_EALIGN
+    assert kvl.kvl_merge_scatter_paged(good, fake, pb, fake, fake, 0, 0, fake) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(good, fake, pb, fake, fake, 1, 2, fake) == kvl.KVL_EINVAL
+    assert kvl.kvl_gather_layer_objects(good, fake, pb, fake, fake, 0, 1, fake, 7) == kvl.KVL_EINVAL
+    assert kvl.kvl_slice_layer(good, fake, pb, fake, 0, 1, 0) == kvl.KVL_EINVAL
     assert kvl.lib().kvl_read_status(None, None, None, None) == kvl.KVL_EINVAL
+
+
+def test_copy_calls_refuse_a_plan_smaller_than_the_geometry_needs(lib):
+    """A copy call is told the plan buffer's size; below the smallest plan of the
+    geometry (kvl_plan_layout(geom, 0)[8]: header, one record per pool block, work
+    list and counters) it returns KVL_EINVAL on the host, before any launch, for every
+    op; at exactly that size the host lets it through to its remaining checks."""
+    g = kvl.geom(2, 2, 16, 256, 64)
+    fake = 1 << 20  # never dereferenced: each call below is refused on the host
+    least = kvl.kvl_plan_layout(g, 0)[8]
+    assert least < kvl.kvl_plan_layout(g, 5)[8]  # a plan of requests needs more
+    assert least >= 256 + 128 * 64  # covers every item record a copy CTA reads first
+    for pb in (0, 16, 256, least - 1):
+        assert kvl.kvl_slice_layer(g, fake, pb, fake, 0, 1, fake) == kvl.KVL_EINVAL
+        assert kvl.kvl_merge_scatter_paged(g, fake, pb, fake, fake, 0, 1, fake) == kvl.KVL_EINVAL
+        for direction in (kvl.KVL_GATHER, kvl.KVL_SCATTER_BACK):
+            assert kvl.kvl_gather_layer_objects(g, fake, pb, fake, fake, 0, 1, fake,
+                                                direction) == kvl.KVL_EINVAL
+    # at the least size the size check passes: a misaligned pool is what answers now
+    assert kvl.kvl_merge_scatter_paged(g, fake, least, fake, fake, 0, 1, fake + 4) == kvl.KVL_EALIGN
+    assert kvl.kvl_merge_scatter_paged(g, fake, least - 1, fake, fake, 0, 1, fake + 4) == kvl.KVL_EINVAL
 
 
 def test_request_packing_follows_layouts():

@@ -143,37 +143,51 @@ def test_host_side_checks_return_without_launching():
     gb.plan()
     g, plan, reqs, tabs = gb.g, gb.d_plan.data_ptr(), gb.d_reqs.data_ptr(), gb.tables.data_ptr()
     pool = d.pool.data_ptr()
+    pb = gb.plan_bytes
     s = torch.cuda.current_stream().cuda_stream
-    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, SPEC.L, 1, pool, None, None, s) == kvl.KVL_EINVAL
-    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, -1, 1, pool, None, None, s) == kvl.KVL_EINVAL
-    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, SPEC.L + 1, pool, None, None, s) == kvl.KVL_EINVAL
-    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool + 8, None, None, s) == kvl.KVL_EALIGN
-    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, 0, None, None, s) == kvl.KVL_EINVAL
-    assert kvl.kvl_gather_layer_objects(g, plan, reqs, tabs, 0, 1, pool, 2, None, s) == kvl.KVL_EINVAL
-    assert kvl.kvl_slice_layer(g, plan, reqs, 0, 1, 0, None, s) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(g, plan, pb, reqs, tabs, SPEC.L, 1, pool, None, None, s) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(g, plan, pb, reqs, tabs, -1, 1, pool, None, None, s) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(g, plan, pb, reqs, tabs, 0, SPEC.L + 1, pool, None, None, s) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(g, plan, pb, reqs, tabs, 0, 1, pool + 8, None, None, s) == kvl.KVL_EALIGN
+    assert kvl.kvl_merge_scatter_paged(g, plan, pb, reqs, tabs, 0, 1, 0, None, None, s) == kvl.KVL_EINVAL
+    assert kvl.kvl_gather_layer_objects(g, plan, pb, reqs, tabs, 0, 1, pool, 2, None, s) == kvl.KVL_EINVAL
+    assert kvl.kvl_slice_layer(g, plan, pb, reqs, 0, 1, 0, None, s) == kvl.KVL_EINVAL
     assert kvl.kvl_batch_plan(g, gb.n_req, reqs, tabs, 1, plan, gb.plan_bytes - 1, s) == kvl.KVL_EINVAL
+    # a plan buffer smaller than the geometry's smallest plan: refused on the host, for
+    # every op, with nothing launched (pool and status untouched)
+    least = kvl.kvl_plan_layout(g, 0)[8]
+    before = d.pool.clone()
+    for small in (16, least - 16):
+        assert kvl.kvl_slice_layer(g, plan, small, reqs, 0, 1, pool, None, s) == kvl.KVL_EINVAL
+        assert kvl.kvl_merge_scatter_paged(g, plan, small, reqs, tabs, 0, 1, pool, None, None,
+                                           s) == kvl.KVL_EINVAL
+        for direction in (kvl.KVL_GATHER, kvl.KVL_SCATTER_BACK):
+            assert kvl.kvl_gather_layer_objects(g, plan, small, reqs, tabs, 0, 1, pool, direction,
+                                                None, s) == kvl.KVL_EINVAL
+    torch.cuda.synchronize()
+    assert torch.equal(d.pool, before) and gb.status() == (0, 0)
     bad = kvl.geom(SPEC.L, SPEC.P, SPEC.B, 24, SPEC.n_pool)
-    assert kvl.kvl_merge_scatter_paged(bad, plan, reqs, tabs, 0, 1, pool, None, None, s) == kvl.KVL_EALIGN
+    assert kvl.kvl_merge_scatter_paged(bad, plan, pb, reqs, tabs, 0, 1, pool, None, None, s) == kvl.KVL_EALIGN
     # launch options: a negative CTA cap, an unknown flag, both host flags
-    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, -1, s) == kvl.KVL_EINVAL
-    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(4, 32),
+    assert kvl.kvl_merge_scatter_paged(g, plan, pb, reqs, tabs, 0, 1, pool, None, -1, s) == kvl.KVL_EINVAL
+    assert kvl.kvl_merge_scatter_paged(g, plan, pb, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(4, 32),
                                        s) == kvl.KVL_EINVAL
-    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 3),
+    assert kvl.kvl_merge_scatter_paged(g, plan, pb, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 3),
                                        s) == kvl.KVL_EINVAL
-    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 7),
+    assert kvl.kvl_merge_scatter_paged(g, plan, pb, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 7),
                                        s) == kvl.KVL_EINVAL
-    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 16),
+    assert kvl.kvl_merge_scatter_paged(g, plan, pb, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 16),
                                        s) == kvl.KVL_EINVAL
-    assert kvl.kvl_merge_scatter_paged(g, plan, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 11),
+    assert kvl.kvl_merge_scatter_paged(g, plan, pb, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 11),
                                        s) == kvl.KVL_EINVAL
     # a NULL request array is for plans of no requests: this plan refuses it on the device
-    assert kvl.kvl_merge_scatter_paged(g, plan, 0, tabs, 0, 1, pool, None, None, s) == kvl.KVL_OK
+    assert kvl.kvl_merge_scatter_paged(g, plan, pb, 0, tabs, 0, 1, pool, None, None, s) == kvl.KVL_OK
     assert gb.status()[0] == kvl.KVL_EINVAL
     gb.plan()
     assert gb.status() == (0, 0)
     # a plan built for another pool size is refused on the device
     other = kvl.geom(SPEC.L, SPEC.P, SPEC.B, SPEC.Rp, SPEC.n_pool - 1)
-    assert kvl.kvl_merge_scatter_paged(other, plan, reqs, tabs, 0, 1, pool, None, None, s) == kvl.KVL_OK
+    assert kvl.kvl_merge_scatter_paged(other, plan, pb, reqs, tabs, 0, 1, pool, None, None, s) == kvl.KVL_OK
     assert gb.status()[0] == kvl.KVL_EINVAL
     # ... and so is one built for another row size or plane count (the boxes of its
     # tensor maps hold the plan's rows); the call copies nothing
@@ -182,11 +196,44 @@ def test_host_side_checks_return_without_launching():
         gb.plan()
         assert gb.status() == (0, 0)
         before = d.pool.clone()
-        assert kvl.kvl_merge_scatter_paged(other, plan, reqs, tabs, 0, 1, pool, None, None,
+        assert kvl.kvl_merge_scatter_paged(other, plan, pb, reqs, tabs, 0, 1, pool, None, None,
                                            s) == kvl.KVL_OK
-        assert kvl.kvl_slice_layer(other, plan, reqs, 0, 1, pool, None, s) == kvl.KVL_OK
+        assert kvl.kvl_slice_layer(other, plan, pb, reqs, 0, 1, pool, None, s) == kvl.KVL_OK
         assert gb.status()[0] == kvl.KVL_EINVAL
         assert torch.equal(d.pool, before)
+
+
+def test_a_plan_holding_more_requests_than_the_stated_buffer_is_refused_on_the_device():
+    """plan_bytes at least the geometry's smallest plan passes the host check, but the
+    plan in the buffer records n_req requests whose sections end beyond plan_bytes: the
+    kernels see that in the header, record KVL_EINVAL and read none of those sections;
+    every buffer keeps its bytes.  The same plan with its full size then copies."""
+    hb = host_buffers(SPEC)
+    gb, d = device_batch(SPEC, hb)
+    gb.plan()
+    g, plan, reqs, tabs = gb.g, gb.d_plan.data_ptr(), gb.d_reqs.data_ptr(), gb.tables.data_ptr()
+    s = torch.cuda.current_stream().cuda_stream
+    least, need = kvl.kvl_plan_layout(g, 0)[8], kvl.kvl_plan_layout(g, gb.n_req)[8]
+    assert least < need <= gb.plan_bytes
+    out = torch.full((gb.total_hit * SPEC.R + 64,), 0x3C, dtype=torch.uint8, device="cuda")
+    pool0, obj0, out0 = d.pool.clone(), d.objects.clone(), out.clone()
+    for short in (least, need - 16):
+        gb.plan()
+        assert kvl.kvl_slice_layer(g, plan, short, reqs, 0, 1, out.data_ptr(), None, s) == kvl.KVL_OK
+        assert kvl.kvl_merge_scatter_paged(g, plan, short, reqs, tabs, 0, 1, d.pool.data_ptr(),
+                                           None, None, s) == kvl.KVL_OK
+        assert kvl.kvl_gather_layer_objects(g, plan, short, reqs, tabs, 0, 1, d.pool.data_ptr(),
+                                            kvl.KVL_GATHER, None, s) == kvl.KVL_OK
+        assert gb.status()[0] == kvl.KVL_EINVAL
+        assert torch.equal(d.pool, pool0) and torch.equal(d.objects, obj0) and torch.equal(out, out0)
+    gb.plan()
+    assert kvl.kvl_merge_scatter_paged(g, plan, need, reqs, tabs, 0, 1, d.pool.data_ptr(), None,
+                                       None, s) == kvl.KVL_OK
+    ob = oracle.Batch(geom_of(SPEC), hb.layout.requests, hb.hit, hb.miss, hb.objects, hb.tables,
+                      hb.src_tables)
+    assert ob.merge_scatter(0, hb.pool)[0] == 0
+    assert np.array_equal(d.pool.cpu().numpy(), hb.pool)
+    assert gb.status() == (0, 0)
 
 
 def test_a_wait_that_runs_out_reports_a_timeout_and_the_context_survives():

@@ -263,7 +263,7 @@ def test_rows_larger_than_a_stage_are_refused():
     gb.plan()
     out = sentinel_dev(ob.total_hit() * spec.R)
     s = torch.cuda.current_stream().cuda_stream
-    assert kvl.kvl_slice_layer(gb.g, gb.d_plan.data_ptr(), gb.d_reqs.data_ptr(), 0, 1,
+    assert kvl.kvl_slice_layer(gb.g, gb.d_plan.data_ptr(), gb.plan_bytes, gb.d_reqs.data_ptr(), 0, 1,
                                out.data_ptr(), None, s) == kvl.KVL_EINVAL
     gb.merge_scatter(0, d.pool)
     assert ob.merge_scatter(0, hb.pool)[0] == 0

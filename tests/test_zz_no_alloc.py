@@ -84,9 +84,9 @@ def test_static_scratch_plan_equals_kvl_batch_plan_on_two_calls():
     pool_ref = d.pool.clone()
     for layer in range(SPEC.L):
         gb.merge_scatter(layer, pool_ref)
-        assert kvl.kvl_merge_scatter_paged(gb.g, small.data_ptr(), gb.d_reqs.data_ptr(),
-                                           gb.tables.data_ptr(), layer, 1, d.pool.data_ptr(),
-                                           None, None, stream) == kvl.KVL_OK
+        assert kvl.kvl_merge_scatter_paged(gb.g, small.data_ptr(), small.numel(),
+                                           gb.d_reqs.data_ptr(), gb.tables.data_ptr(), layer, 1,
+                                           d.pool.data_ptr(), None, None, stream) == kvl.KVL_OK
     torch.cuda.synchronize()
     assert torch.equal(d.pool, pool_ref)
     assert kvl.kvl_read_status(small.data_ptr(), stream) == (0, 0)
