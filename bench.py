@@ -1,4 +1,5 @@
-"""Benchmark of the layer-wise paged KV block reshuffle on one GB300 (or N replicas).
+"""Benchmark of the layer-wise paged KV block reshuffle on one GB300 (or one batch split
+over N GPUs).
 
 One step = the whole hot path over one batch: the batch plan, then for every layer
 slice (hit_layer[l]), merge-scatter (hit + miss into the paged pool), gather (pool ->
@@ -6,18 +7,31 @@ per-layer K/V objects) and scatter-back (objects -> pool).  The ops run phase by
 phase (all layers of one op, then the next op), so no kernel finds its inputs in L2:
 every phase streams at least 8 GB through a 129 MB L2.
 
-Prints one JSON line.  `value` is algorithmic bytes moved (read + write, every op)
-per second of the timed region, in GB/s; `roofline` is the dominant kernel's
-achieved bandwidth against the measured HBM copy peak; `e2e` repeats the step with
-the inputs copied from pinned host memory and the objects read back inside the timed
-region; `cpu_baseline` is the CPU oracle on a bounded sample of the same workload.
+Prints one JSON line for the headline workload (default: the 256-request batch, the
+largest workload that fits one GPU).  `value` is algorithmic bytes moved (read +
+write, every op) per second of the timed region, in GB/s; `roofline` is the dominant
+kernel's achieved bandwidth against the measured HBM copy peak; `e2e` repeats the
+step through the C ABI with the inputs copied from pinned host memory and the objects
+read back inside the timed region (and a variant whose slice and merge-scatter read
+the pinned host inputs in place); `cpu_baseline` is the CPU oracle on a bounded sample
+of the same workload; `serial` is the step with every launch waiting for the one
+before it.  `config.per_workload` gives the same step figures for the other full-size
+workloads, measured in the same process after the headline, and `host_leg` and
+`overlap` the host-buffer legs and the layer-wise pipeline beside compute under an SM
+budget, on the Llama-3-8B-shaped turn.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference   # the CPU oracle on the host cores
+
+With N > 1 (one process per GPU under torchrun) the batch is split: each rank takes a
+contiguous run of requests (or of layers, for fewer requests than ranks), with its
+own pool, plan and objects, and no data-path exchange; `value` is the bytes all ranks
+moved over the slowest rank's time.
 """
 from __future__ import annotations
 
 import argparse
+import contextlib
 import copy
 import dataclasses
 import hashlib
@@ -40,14 +54,35 @@ import workloads  # noqa: E402
 
 METRIC = "KV reshuffle HBM GB/s (read+write) and % of GB300 peak; µs per layer"
 UNIT = "GB/s"
-DEFAULT_WORKLOAD = "llama3_8b_agentic"
+DEFAULT_WORKLOAD = "many_small"
+SIDE_WORKLOADS = ("llama3_8b_agentic", "qwen3_32b_long", "latent_batch")
+PIPELINE_WORKLOAD = "llama3_8b_agentic"  # host legs and the overlap with compute
 FALLBACK_HBM_GBS = 6800.0
-NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, vendor figure (context for "% of peak")
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, about 8 TB/s (context for "% of peak")
 HIT_RING = 8
 KERNEL_REPS = 11  # replays whose per-phase events give the per-kernel median
 OPS = ("slice", "merge_scatter", "gather", "scatter_back")
 KERNEL_NAMES = {"slice": "kvl_slice_kernel", "merge_scatter": "kvl_merge_scatter_kernel",
                 "gather": "kvl_gather_kernel", "scatter_back": "kvl_scatter_back_kernel"}
+_T0 = time.perf_counter()
+
+
+def host_available() -> int:
+    """Bytes of host memory the kernel reports available (MemAvailable), or 0."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def log(msg: str) -> None:
+    """A progress line on stderr (stdout carries only the JSON line)."""
+    print(f"[bench {time.perf_counter() - _T0:7.1f} s] {msg} (host memory available "
+          f"{host_available() / 1e9:.0f} GB)", file=sys.stderr, flush=True)
 
 
 # ---------------------------------------------------------------------------
@@ -80,13 +115,15 @@ def describe(spec) -> dict:
              step="plan, then per layer slice, merge-scatter, gather, scatter-back "
                   "(each op over all layers before the next op)",
              l2="inputs larger than L2: every phase streams >= 8 GB past a 129 MB L2")
-    if spec.name == "llama3_8b_agentic":
+    if spec.P == 2 and spec.Rp == 2048:
         d.update(H_kv=8, d=128)
+    if spec.part:
+        d.update(part=spec.part)
     return d
 
 
 # ---------------------------------------------------------------------------
-# Multi-rank plumbing (one process per GPU; replicas, no data-path collective)
+# Multi-rank plumbing (one process per GPU; the batch split, no data-path collective)
 # ---------------------------------------------------------------------------
 
 def dist_env():
@@ -114,6 +151,25 @@ def max_over_ranks(value: float, dist, device=None) -> float:
     t = torch.tensor([value], dtype=torch.float64, device=device or "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def sum_over_ranks(value: float, dist, device=None) -> float:
+    """Sum of a value over all ranks (the bytes every rank moved)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def rank_part(spec, world, rank):
+    """(Part, its spec) of `rank` when `spec`'s batch is split over `world` GPUs
+    (layer_wise_paged_gb300.shard); the spec is None for a rank left idle."""
+    from layer_wise_paged_gb300.shard import split_batch
+    part = split_batch(spec.t_hit, spec.t_miss, spec.B, spec.L, workloads.block_tables(spec),
+                       workloads.source_tables(spec), world, rank)
+    return part, workloads.part_spec(spec, part)
 
 
 def barrier(dist, device=None):
@@ -288,8 +344,13 @@ class OracleSample:
         self.objects = np.full(max(16, self.lay.obj_bytes), workloads.SENTINEL, np.uint8)
 
     def worker_bytes(self) -> int:
-        """Host bytes one more worker allocates."""
-        return self.pool.nbytes + self.objects.nbytes
+        """Host bytes one more worker holds while it runs a layer: its own pool and
+        objects, plus what one layer's calls allocate while they run (the slice's
+        output, and the hit_layer and complete_layer buffers the oracle's merge-scatter
+        builds before it scatters)."""
+        spec = self.spec
+        n_hit, n_all = int(sum(spec.t_hit)), int(spec.t_all().sum())
+        return self.pool.nbytes + self.objects.nbytes + (2 * n_hit + n_all) * spec.R
 
     def worker(self) -> "OracleSample":
         w = copy.copy(self)
@@ -328,14 +389,14 @@ def host_cpu() -> str:
 
 def oracle_threads(sample, want=None) -> int:
     """Worker threads for the oracle: every host core, as far as host memory allows
-    (half of what is available goes to the workers' own pools and objects)."""
+    (at most 60 % of the memory available now goes to the workers, each counted with
+    everything it holds while it runs a layer)."""
     cores = os.cpu_count() or 1
     want = cores if want is None else max(1, min(int(want), cores))
-    try:
-        avail = os.sysconf("SC_AVPHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
-    except (ValueError, OSError):
+    avail = host_available()
+    if avail <= 0:
         return 1
-    return max(1, min(want, int(avail // 2 // max(1, sample.worker_bytes()))))
+    return max(1, min(want, int(avail * 0.6 // max(1, sample.worker_bytes()))))
 
 
 def oracle_workers(sample, threads):
@@ -375,6 +436,7 @@ def cpu_baseline(spec, budget_s=12.0, sample=None, threads=None):
     (at least one layer).  The all-cores figure is the baseline's value."""
     sample = sample or OracleSample(spec)
     n = oracle_threads(sample, threads)
+    log(f"cpu baseline: {n} oracle threads, {sample.worker_bytes() / 1e9:.1f} GB each")
     workers = oracle_workers(sample, n)
     layers = [i % spec.L for i in range(spec.L * 1000)]
     b1, t1, l1 = time_oracle(workers[:1], layers, budget_s / 2)
@@ -389,11 +451,16 @@ def cpu_baseline(spec, budget_s=12.0, sample=None, threads=None):
 
 
 def bench_spec(args):
-    """The named workload, or its first --layers layers (a smaller case of the same
-    kernels, for profiling captures that must fit in a few GB)."""
+    """The named workload, or its first --layers layers and first --requests requests
+    (a smaller case of the same kernels, for profiling captures that must fit in a few
+    GB; a batch cut to fewer requests gets a pool of 1.25 times the blocks they use)."""
     spec = workloads.get_spec(args.workload)
     if args.layers:
         spec = dataclasses.replace(spec, L=min(spec.L, args.layers))
+    if args.requests and args.requests < spec.n_req:
+        n = args.requests
+        spec = dataclasses.replace(spec, t_hit=spec.t_hit[:n], t_miss=spec.t_miss[:n])
+        spec = dataclasses.replace(spec, n_pool=int(-(-5 * int(spec.nblk().sum()) // 4)))
     if args.objects != spec.objects:
         spec = dataclasses.replace(spec, objects=args.objects)
     return spec
@@ -520,56 +587,69 @@ def capture_step_graph(dev, stream, fn):
     return graph
 
 
-def run_gpu(args):
+# ---------------------------------------------------------------------------
+# Measurements on one GPU
+# ---------------------------------------------------------------------------
+
+def make_event():
+    """A timing event that becomes a record node when captured in a CUDA graph (None if
+    this torch has no external events)."""
     import torch
-    import layer_wise_paged_gb300 as kvl
-    from layer_wise_paged_gb300.batch import Batch
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return None
 
-    world, rank, local = dist_env()
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py: no CUDA device (the GPU arm has no CPU fallback)")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    dist = init_dist(world, "nccl")
-    kvl.build()
-    kvl.lib()
 
-    spec = bench_spec(args)
-    bs = BenchStep(spec, dev, layers_per_launch=args.layers_per_launch,
-                   serial=args.serial_launches)
-    bufs, lay, g, batch = bs.bufs, bs.bufs["layout"], bs.geom, bs.batch
-    K, groups, ring, one_layer = bs.K, bs.groups, bs.ring, bs.one_layer
-    launch_flags = bs.flags
-    stream = torch.cuda.current_stream(dev)
-
-    def make_event():
-        try:  # a record node when captured in a CUDA graph
-            return torch.cuda.Event(enable_timing=True, external=True)
-        except TypeError:
-            return None
-
-    def run_step(b, s, events):
-        bs.enqueue(b, s, events)
-
-    def step(events=None, s=None):
-        run_step(batch, s or stream, events)
-
-    launches_per_step = kvl.kvl_launches_per_call(0) + len(groups) * 4
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
+def check_status(batch, stream, when):
     code, detail = batch.status(stream)
     if code != 0:
-        raise SystemExit(f"bench.py: plan status {code} detail {detail}")
+        raise SystemExit(f"bench.py: plan status {code} detail {detail} {when}")
 
-    # One step captured as a CUDA graph (the launches of the C-ABI calls, with a
-    # timing event recorded on the launch stream around each kernel), replayed once
-    # per timed step.  --eager launches through the C ABI from Python every step.
-    ev = None
-    graph = None
-    if not args.eager and make_event() is not None:
+
+def steps_for(spec, seconds, lo=10, hi=200):
+    """Steps of `spec` that take about `seconds` at 6.5 TB/s (at least lo, at most hi)."""
+    return int(min(hi, max(lo, seconds * 6.5e12 / max(1, step_bytes(spec)))))
+
+
+def per_op_figures(spec, groups, phase_s):
+    """Per-op launch duration (median over samples of phase time / launches), GB/s and
+    layers/s, and the dominant op (largest phase time)."""
+    per_op = {}
+    for op in OPS:
+        avg = statistics.median(t / len(groups) for t in phase_s[op])
+        per_op[op] = {"us_per_launch": round(avg * 1e6, 2),
+                      "gbs": round(op_bytes(spec)[op] * spec.L / len(groups) / avg / 1e9, 1),
+                      "layers_per_s": round(spec.L / len(groups) / avg, 1),
+                      "total_s": avg * len(groups)}
+    dom = max(OPS, key=lambda o: per_op[o]["total_s"])
+    return per_op, dom
+
+
+def measure_step(spec, dev, *, steps, warmup, serial=False, layers_per_launch=1, eager=False,
+                 clocks=None, dist=None, kernel_reps=KERNEL_REPS, bs=None):
+    """`warmup` untimed bench steps of `spec`, then `steps` timed ones (CUDA events on
+    the launch stream, max over ranks), each a replay of a CUDA graph of one step (or,
+    with `eager`, C-ABI calls from Python).  Per-op launch durations come from events
+    around each op's phase of launches: the median of `kernel_reps` replays after the
+    timed region (a graph's events hold its last replay), or of the timed steps.
+    `bs`: the BenchStep of an earlier measurement of the same workload to reuse (its
+    buffers; `serial` replaces its launch rule), else a new one is allocated.
+    Returns a dict with the BenchStep (`bs`), `elapsed` (s), `per_op`, `dom` and how
+    the step was launched."""
+    import torch
+    if bs is None:
+        bs = BenchStep(spec, dev, layers_per_launch=layers_per_launch, serial=serial)
+    bs.serial = serial
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        bs.enqueue(bs.batch, stream)
+    torch.cuda.synchronize(dev)
+    check_status(bs.batch, stream, "after the warm-up steps")
+    graph, ev = None, None
+    if not eager and make_event() is not None:
         ev = {op: (make_event(), make_event()) for op in OPS}
-        graph = capture_step_graph(dev, stream, lambda s_: run_step(batch, s_, ev))
+        graph = capture_step_graph(dev, stream, lambda s_: bs.enqueue(bs.batch, s_, ev))
         for _ in range(2):
             graph.replay()
         torch.cuda.synchronize(dev)
@@ -581,274 +661,373 @@ def run_gpu(args):
         else:
             evs = {op: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for op in OPS}
-            step(evs)
+            bs.enqueue(bs.batch, stream, evs)
             for op in OPS:
                 eager_ev[op].append(evs[op])
 
-    clocks_path = Path(args.clocks_csv) if args.clocks_csv else None
     barrier(dist, dev)
     torch.cuda.synchronize(dev)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local, clocks_path) as clk:
-        time.sleep(0.3)
+    with (clocks if clocks is not None else contextlib.nullcontext()):
+        if clocks is not None:
+            time.sleep(0.3)
         t0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             timed_step()
         t1.record(stream)
         torch.cuda.synchronize(dev)
     barrier(dist, dev)
-    elapsed = t0.elapsed_time(t1) / 1e3
-    elapsed = max_over_ranks(elapsed, dist, dev)
-    code, detail = batch.status(stream)
-    if code != 0:
-        raise SystemExit(f"bench.py: status {code} detail {detail} after the timed steps")
-    # per-launch durations: each op's phase time over its launches, the median over
-    # timed steps.  Eager mode keeps every timed step's events; a graph's events hold
-    # its last replay, so after the timed region the graph is replayed KERNEL_REPS more
-    # times, each read back on its own (these replays are not part of `value`).
+    elapsed = max_over_ranks(t0.elapsed_time(t1) / 1e3, dist, dev)
+    check_status(bs.batch, stream, "after the timed steps")
     if graph is not None:
         phase_s = {op: [] for op in OPS}
-        for _ in range(KERNEL_REPS):
+        for _ in range(kernel_reps):
             graph.replay()
             torch.cuda.synchronize(dev)
             for op in OPS:
                 phase_s[op].append(ev[op][0].elapsed_time(ev[op][1]) / 1e3)
-        code, detail = batch.status(stream)
-        if code != 0:
-            raise SystemExit(f"bench.py: status {code} detail {detail} after the timing replays")
+        check_status(bs.batch, stream, "after the timing replays")
     else:
         phase_s = {op: [a.elapsed_time(b) / 1e3 for a, b in eager_ev[op]] for op in OPS}
+    per_op, dom = per_op_figures(spec, bs.groups, phase_s)
+    del graph
+    return dict(bs=bs, elapsed=elapsed, steps=steps, per_op=per_op, dom=dom,
+                launch="CUDA graph of one step, replayed per step" if ev is not None
+                else "eager C-ABI calls from Python",
+                kernel_timing="CUDA events around each op's phase of launches (launch duration "
+                f"= phase time / launches), median of {kernel_reps} graph replays after the "
+                "timed region" if ev is not None else
+                "CUDA events around each op's phase of launches, median over the timed steps")
 
+
+def dominant_kernel(m):
+    """The dominant op's kernel name, with the pipeline depth most of its launches ran
+    with (3 stages when sharing SMs with a neighbour launch, else 6)."""
+    bs, dom = m["bs"], m["dom"]
+    shares = bs.flags(dom, 1, bs.groups[1][0]) if len(bs.groups) > 1 else 0
+    return f"{KERNEL_NAMES[dom]}<{3 if shares else 6}>"
+
+
+def roofline_of(spec, m, peak, peak_kind):
+    """The dominant kernel against the measured copy peak (and the nominal HBM figure);
+    traffic from the committed ncu record when it was taken on this kernel source."""
+    bs, dom = m["bs"], m["dom"]
+    kname = dominant_kernel(m)
+    achieved = m["per_op"][dom]["gbs"]
+    traffic = recorded_traffic(kname, spec.name) if bs.K == 1 and not spec.part else None
+    return {"bound": "hbm", "kernel": kname + f" ({dom})", "achieved": achieved, "peak": peak,
+            "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+            "nominal_peak": NOMINAL_HBM_GBS,
+            "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+            "algorithmic_bytes_per_launch": op_bytes(spec)[dom] * spec.L // len(bs.groups),
+            "traffic": traffic,
+            "traffic_source": "profiles/dram_traffic.txt (ncu dram__bytes_read.sum + "
+                              "dram__bytes_write.sum per launch, this kernel source)"
+            if traffic is not None else None}
+
+
+def step_summary(spec, m, peak):
+    """The figures of one measured step: GB/s, µs per layer, per-op kernels, the
+    dominant kernel's fraction of the measured and nominal peaks."""
     sb = step_bytes(spec)
-    value = world * sb * args.steps / elapsed / 1e9
-    per_op = {}
-    for op in OPS:
-        ts = [t / len(groups) for t in phase_s[op]]
-        avg = statistics.median(ts)
-        per_op[op] = {"us_per_launch": round(avg * 1e6, 2),
-                      "gbs": round(op_bytes(spec)[op] * spec.L / len(groups) / avg / 1e9, 1),
-                      "layers_per_s": round(spec.L / len(groups) / avg, 1),
-                      "total_s": avg * len(groups)}
-    dom = max(OPS, key=lambda o: per_op[o]["total_s"])
-    peak, peak_kind = hbm_peak()
-    achieved = per_op[dom]["gbs"]
-    # the pipeline depth most of the dominant op's launches ran with (the kernels are
-    # instantiated per depth: 3 stages when sharing SMs with a neighbour launch, else 6)
-    shares = launch_flags(dom, 1, groups[1][0]) if len(groups) > 1 else 0
-    kname = f"{KERNEL_NAMES[dom]}<{3 if shares else 6}>"
-    traffic = recorded_traffic(kname, spec.name) if K == 1 else None
-    roofline = {"bound": "hbm", "kernel": kname + f" ({dom})",
-                "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-                "nominal_peak": NOMINAL_HBM_GBS,
-                "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
-                "algorithmic_bytes_per_launch": op_bytes(spec)[dom] * spec.L // len(groups),
-                "traffic": traffic}
-    kernels = {op: {k: v for k, v in per_op[op].items() if k != "total_s"} for op in OPS}
-
-    # ---- end to end: pinned host inputs in, objects out, inside the timed region.
-    # Two sets of device inputs and objects: step s uploads into set s % 2 on one copy
-    # stream and reads its objects back on another, so step s+1's upload and step
-    # s-1's read-back overlap step s's kernels.  Every step still copies its own
-    # inputs in and its own objects out inside the timed region.
-    e2e = None
-    if not args.no_e2e:
-        h_hit = torch.empty(bufs["hit"].numel(), dtype=torch.uint8, pin_memory=True)
-        h_miss = torch.empty(bufs["miss"].numel(), dtype=torch.uint8, pin_memory=True)
-        h_tab = torch.empty(bufs["tables"].numel(), dtype=torch.int32, pin_memory=True)
-        h_obj = [torch.empty(bufs["objects"].numel(), dtype=torch.uint8, pin_memory=True)
-                 for _ in range(2)]
-        h_hit.copy_(bufs["hit"])
-        h_miss.copy_(bufs["miss"])
-        h_tab.copy_(bufs["tables"])
-        h_in = h_hit.numel() + h_miss.numel() + 4 * h_tab.numel()
-        h_out = h_obj[0].numel()
-        sets = [dict(hit=bufs["hit"], miss=bufs["miss"], tables=bufs["tables"],
-                     objects=bufs["objects"], batch=batch, graph=graph)]
-        second = dict(hit=torch.empty_like(bufs["hit"]), miss=torch.empty_like(bufs["miss"]),
-                      tables=torch.empty_like(bufs["tables"]),
-                      objects=torch.empty_like(bufs["objects"]))
-        second["batch"] = Batch(g, lay.requests, second["hit"], second["miss"], second["objects"],
-                                second["tables"], bufs["src_tables"])
-        second["graph"] = None
-        if graph is not None:
-            second["graph"] = capture_step_graph(
-                dev, stream, lambda s_: run_step(second["batch"], s_, None))
-        sets.append(second)
-        h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        ev_in = [torch.cuda.Event() for _ in range(2)]
-        ev_comp = [torch.cuda.Event() for _ in range(2)]
-        ev_out = [torch.cuda.Event() for _ in range(2)]
-
-        def e2e_run(n):
-            h2d.wait_stream(stream)
-            d2h.wait_stream(stream)
-            for i in range(n):
-                k = i % 2
-                st = sets[k]
-                if i >= 2:
-                    h2d.wait_event(ev_comp[k])  # step i-2 no longer reads set k's inputs
-                with torch.cuda.stream(h2d):
-                    st["hit"].copy_(h_hit, non_blocking=True)
-                    st["miss"].copy_(h_miss, non_blocking=True)
-                    st["tables"].copy_(h_tab, non_blocking=True)
-                    ev_in[k].record(h2d)
-                stream.wait_event(ev_in[k])
-                if i >= 2:
-                    stream.wait_event(ev_out[k])  # step i-2's objects are on the host
-                if st["graph"] is not None:
-                    st["graph"].replay()
-                else:
-                    run_step(st["batch"], stream, None)
-                ev_comp[k].record(stream)
-                d2h.wait_event(ev_comp[k])
-                with torch.cuda.stream(d2h):
-                    h_obj[k].copy_(st["objects"], non_blocking=True)
-                    ev_out[k].record(d2h)
-            stream.wait_stream(h2d)
-            stream.wait_stream(d2h)
-
-        def link_rates():
-            """The copy engines' rates on this machine for the step's own transfers: inputs
-            in alone, objects out alone, and both at once (GB/s, best of 3)."""
-            def timed(fn):
-                best = None
-                for _ in range(3):
-                    torch.cuda.synchronize(dev)
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                    h2d.wait_stream(stream)
-                    d2h.wait_stream(stream)
-                    fn()
-                    stream.wait_stream(h2d)
-                    stream.wait_stream(d2h)
-                    b.record(stream)
-                    torch.cuda.synchronize(dev)
-                    t = a.elapsed_time(b) / 1e3
-                    best = t if best is None else min(best, t)
-                return best
-
-            def up():
-                with torch.cuda.stream(h2d):
-                    second["hit"].copy_(h_hit, non_blocking=True)
-                    second["miss"].copy_(h_miss, non_blocking=True)
-                    second["tables"].copy_(h_tab, non_blocking=True)
-
-            def down():
-                with torch.cuda.stream(d2h):
-                    h_obj[1].copy_(second["objects"], non_blocking=True)
-
-            t_up, t_down = timed(up), timed(down)
-            t_both = timed(lambda: (up(), down()))
-            return {"h2d_gbs": round(h_in / t_up / 1e9, 1), "d2h_gbs": round(h_out / t_down / 1e9, 1),
-                    "both_gbs": round((h_in + h_out) / t_both / 1e9, 1), "floor_ms_per_step":
-                    round(t_both * 1e3, 3)}
-
-        link = link_rates()
-        e2e_run(2)
-        torch.cuda.synchronize(dev)
-        n_e2e = max(3, min(args.e2e_steps, args.steps))
-        barrier(dist, dev)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        e2e_run(n_e2e)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        et = max_over_ranks(e0.elapsed_time(e1) / 1e3, dist, dev)
-        code, detail = second["batch"].status(stream)
-        if code != 0:
-            raise SystemExit(f"bench.py: status {code} detail {detail} in the end-to-end steps")
-        e2e = {"value": round(world * sb * n_e2e / et / 1e9, 2), "unit": UNIT,
-               "h2d_bytes_per_step": int(h_in), "d2h_bytes_per_step": int(h_out),
-               "steps": n_e2e, "ms_per_step": round(et / n_e2e * 1e3, 3),
-               "link": dict(link, frac_of_floor=round(link["floor_ms_per_step"] /
-                                                      (et / n_e2e * 1e3), 4)),
-               "path": "per step: pinned host -> device copies of the full block, miss KV "
-                       "and block tables, the step through the C ABI, objects -> pinned host; "
-                       "two buffer sets, so one step's copies overlap its neighbours' kernels"}
-        del h_hit, h_miss, h_tab, h_obj, sets, second
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sample = OracleSample(spec, hit=bufs["hit"].cpu().numpy(), miss=bufs["miss"].cpu().numpy())
-        cpu = cpu_baseline(spec, args.cpu_seconds, sample)
-
-    if rank == 0:
-        cfg = describe(spec)
-        cfg.update(layers_per_launch=K,
-                   objects="one layer (layer stride 0)" if one_layer else "all layers",
-                   hit_layer_buffers=ring,
-                   us_per_layer=round(elapsed / args.steps / spec.L * 1e6, 2),
-                   layers_per_s=round(world * spec.L * args.steps / elapsed, 1),
-                   launch="CUDA graph of one step, replayed per step" if graph is not None
-                   else "eager C-ABI calls from Python",
-                   kernel_timing="CUDA events around each op's phase of launches (launch "
-                   f"duration = phase time / launches), median of {KERNEL_REPS} graph replays "
-                   "after the timed region" if graph is not None
-                   else "CUDA events around each op's phase of launches, median over the "
-                   "timed steps",
-                   launch_overlap="none: every launch waits for the one before it"
-                   if args.serial_launches else
-                   "as below, except gather and scatter-back (shared object layer), "
-                   "which run one launch at a time: KVL_LAUNCH_OVERLAP_PREVIOUS on a "
-                   "phase's launches after its first, KVL_LAUNCH_SHARE_SMS on the first"
-                   if one_layer else
-                   "KVL_LAUNCH_OVERLAP_PREVIOUS on a phase's launches after its first "
-                   "(each may start beside its predecessor, on half of an SM's shared "
-                   "memory), KVL_LAUNCH_SHARE_SMS on the first",
-                   step_bytes=sb, kernels=kernels, launches_per_step=launches_per_step,
-                   parallelism=f"{world} independent replica(s)", gpu=torch.cuda.get_device_name(dev))
-        line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": round(elapsed / args.steps * 1e3, 4), "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "u8",
-                "data": "synthetic (seeded bf16 KV payload; byte copies)", "config": cfg,
-                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": launches_per_step * args.steps * world,
-                "clocks": clk.summary()}
-        print(json.dumps(line), flush=True)
-    if dist is not None:
-        dist.destroy_process_group()
-    return 0
+    gbs = sb * m["steps"] / m["elapsed"] / 1e9
+    dom = m["dom"]
+    return {"step_gbs": round(gbs, 1), "ms_per_step": round(m["elapsed"] / m["steps"] * 1e3, 4),
+            "us_per_layer": round(m["elapsed"] / m["steps"] / spec.L * 1e6, 2),
+            "layers_per_s": round(spec.L * m["steps"] / m["elapsed"], 1), "steps": m["steps"],
+            "step_frac": round(gbs / peak, 4),
+            "kernels": {op: {k: v for k, v in m["per_op"][op].items() if k != "total_s"}
+                        for op in OPS},
+            "dominant": dominant_kernel(m) + f" ({dom})",
+            "frac": round(m["per_op"][dom]["gbs"] / peak, 4),
+            "frac_of_nominal": round(m["per_op"][dom]["gbs"] / NOMINAL_HBM_GBS, 4)}
 
 
-def run_overlap(args):
-    """Layer-wise pipeline under an SM budget: layer l's merge-scatter (at most k CTAs,
-    i.e. k SMs) on a transfer stream, and a synthetic compute kernel for layer l (a
-    bf16 GEMM standing in for the layer's attention) on a compute stream that waits for
-    layer l's transfer.  Transfers run ahead, so layer l+1's copy overlaps layer l's
-    compute.  For each budget: the transfer alone, the compute alone, the pipeline, and
-    the pipeline's time beyond the compute alone (bubbles plus the slowdown of sharing
-    the GPU), next to Tutti's zero-bubble condition T_transfer <= T_compute
-    (Tutti 阅读笔记, eq. (17))."""
+class EndToEnd:
+    """The bench step through the C ABI with its inputs in pinned host memory (Grace
+    memory, over NVLink-C2C) and its objects read back to pinned host memory, every
+    step, inside the timed region.  Two variants:
+
+    * staged: per step, copy-engine copies of the block tables, the full block and
+      the miss KV into HBM, then the step, with each gathered layer of objects copied
+      back to the host as soon as it exists;
+    * in place: the same, except that the slice and merge-scatter read the full block
+      and the miss KV straight from pinned host memory (KVL_LAUNCH_HOST_SRC: SM loads
+      over the link), so nothing is staged in HBM first.
+
+    Launches are eager C-ABI calls from Python.  Copies run on their own streams: a
+    step's uploads start once the previous step's merge-scatter no longer reads the
+    inputs, and each layer's read-back overlaps the next layer's gather where the
+    objects buffer allows (one shared object layer: a gather waits for the previous
+    layer's read-back)."""
+
+    def __init__(self, bs, dev):
+        import torch
+        from layer_wise_paged_gb300.batch import Batch, MappedHost
+        self.bs, self.dev = bs, dev
+        b = bs.bufs
+        n_obj = b["objects"].numel()
+        slots = 2 if bs.one_layer else 1
+        need = b["hit"].numel() + b["miss"].numel() + slots * n_obj
+        avail = host_available()
+        if need > 0.6 * avail:
+            raise MemoryError(f"pinned host buffers of {need / 1e9:.0f} GB, host memory "
+                              f"available {avail / 1e9:.0f} GB")
+        log(f"end to end: pinning {need / 1e9:.1f} GB of host memory")
+        self.h_hit = MappedHost(b["hit"].numel())
+        self.h_miss = MappedHost(b["miss"].numel())
+        self.h_obj = [MappedHost(n_obj) for _ in range(slots)]
+        log("end to end: host buffers pinned")
+        self.t_hit = torch.from_numpy(self.h_hit.np)[:b["hit"].numel()]
+        self.t_miss = torch.from_numpy(self.h_miss.np)[:b["miss"].numel()]
+        self.t_hit.copy_(b["hit"])
+        self.t_miss.copy_(b["miss"])
+        self.h_tab = torch.empty(b["tables"].numel(), dtype=torch.int32, pin_memory=True)
+        self.h_tab.copy_(b["tables"])
+        log("end to end: host inputs written")
+        self.t_obj = [torch.from_numpy(h.np)[:n_obj] for h in self.h_obj]
+        spec, lay = bs.spec, b["layout"]
+        g = (spec.L, spec.P, spec.B, spec.Rp, spec.n_pool)
+        # the in-place batch: the same requests, their hit and miss rows at the mapped
+        # host addresses
+        self.b_host = Batch(g, lay.requests, self.h_hit, self.h_miss, b["objects"], b["tables"],
+                            b["src_tables"])
+        self.main = torch.cuda.current_stream(dev)
+        self.h2d, self.d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        self.ev_in, self.ev_free, self.ev_g, self.ev_out = (torch.cuda.Event() for _ in range(4))
+        self.h2d_bytes = b["hit"].numel() + b["miss"].numel() + 4 * b["tables"].numel()
+        self.reads_back = spec.L if bs.one_layer else 1
+        self.d2h_bytes = n_obj * self.reads_back
+        # bytes the in-place slice and merge-scatter read across the link per step
+        self.in_place_bytes = (op_bytes(spec)["slice"] + op_bytes(spec)["merge_scatter"]) // 2 * spec.L
+
+    def _read_back(self, slot):
+        import torch
+        self.ev_g.record(self.main)
+        self.d2h.wait_event(self.ev_g)
+        with torch.cuda.stream(self.d2h):
+            self.t_obj[slot].copy_(self.bs.bufs["objects"], non_blocking=True)
+        self.ev_out.record(self.d2h)
+
+    def _step(self, in_place):
+        import torch
+        import layer_wise_paged_gb300 as kvl
+        bs, s, b = self.bs, self.main, self.bs.bufs
+        batch = self.b_host if in_place else bs.batch
+        # inputs: uploaded once the previous step's merge-scatter no longer reads them
+        self.h2d.wait_event(self.ev_free)
+        with torch.cuda.stream(self.h2d):
+            b["tables"].copy_(self.h_tab, non_blocking=True)
+            if not in_place:
+                b["hit"].copy_(self.t_hit, non_blocking=True)
+                b["miss"].copy_(self.t_miss, non_blocking=True)
+        self.ev_in.record(self.h2d)
+        s.wait_event(self.ev_in)
+        batch.plan(stream=s)
+        host = kvl.KVL_LAUNCH_HOST_SRC
+        for i, (l0, n) in enumerate(bs.groups):
+            batch.slice_layer(l0, bs.hit_views[l0], s, layer_count=n,
+                              flags=host if in_place else bs.flags("slice", i, l0))
+        for i, (l0, n) in enumerate(bs.groups):
+            batch.merge_scatter(l0, bs.pool, None, s, layer_count=n,
+                                flags=host if in_place else bs.flags("merge_scatter", i, l0))
+        self.ev_free.record(s)
+        for i, (l0, n) in enumerate(bs.groups):
+            if bs.one_layer or i == 0:
+                s.wait_event(self.ev_out)  # the objects buffer has been read back
+            batch.gather(l0, bs.pool, s, layer_count=n, flags=bs.flags("gather", i, l0))
+            if bs.one_layer:
+                self._read_back(i % 2)
+        if not bs.one_layer:
+            self._read_back(0)
+        for i, (l0, n) in enumerate(bs.groups):
+            batch.scatter_back(l0, bs.pool, s, layer_count=n, flags=bs.flags("scatter_back", i, l0))
+
+    def run(self, n, in_place):
+        """n steps; returns seconds (CUDA events on the launch stream)."""
+        import torch
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(self.dev)
+        e0.record(self.main)
+        self.ev_free.record(self.main)
+        self.ev_out.record(self.main)
+        for _ in range(n):
+            self._step(in_place)
+        self.main.wait_stream(self.h2d)
+        self.main.wait_stream(self.d2h)
+        e1.record(self.main)
+        torch.cuda.synchronize(self.dev)
+        check_status(self.b_host if in_place else self.bs.batch, self.main,
+                     "in the end-to-end steps")
+        return e0.elapsed_time(e1) / 1e3
+
+    def link_rates(self, reps=2):
+        """The copy engines' rates on this machine for the step's own transfers: inputs in
+        alone, objects out alone (as the step reads them back), and both at once."""
+        import torch
+        b = self.bs.bufs
+
+        def timed(fn):
+            best = None
+            for _ in range(reps):
+                torch.cuda.synchronize(self.dev)
+                a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(self.main)
+                self.h2d.wait_stream(self.main)
+                self.d2h.wait_stream(self.main)
+                fn()
+                self.main.wait_stream(self.h2d)
+                self.main.wait_stream(self.d2h)
+                z.record(self.main)
+                torch.cuda.synchronize(self.dev)
+                t = a.elapsed_time(z) / 1e3
+                best = t if best is None else min(best, t)
+            return best
+
+        def up():
+            with torch.cuda.stream(self.h2d):
+                b["tables"].copy_(self.h_tab, non_blocking=True)
+                b["hit"].copy_(self.t_hit, non_blocking=True)
+                b["miss"].copy_(self.t_miss, non_blocking=True)
+
+        def down():
+            with torch.cuda.stream(self.d2h):
+                for k in range(self.reads_back):
+                    self.t_obj[k % len(self.t_obj)].copy_(b["objects"], non_blocking=True)
+
+        t_up, t_down = timed(up), timed(down)
+        t_both = timed(lambda: (up(), down()))
+        return {"h2d_gbs": round(self.h2d_bytes / t_up / 1e9, 1),
+                "d2h_gbs": round(self.d2h_bytes / t_down / 1e9, 1),
+                "both_gbs": round((self.h2d_bytes + self.d2h_bytes) / t_both / 1e9, 1),
+                "floor_ms_per_step": round(t_both * 1e3, 3)}
+
+    @staticmethod
+    def floor_s(link, bytes_in, bytes_out):
+        """The least time the link allows for these bytes at the copy engines' measured
+        rates: each direction alone, and both together."""
+        return max(bytes_in / (link["h2d_gbs"] * 1e9), bytes_out / (link["d2h_gbs"] * 1e9),
+                   (bytes_in + bytes_out) / (link["both_gbs"] * 1e9))
+
+    def measure(self, steps, dist=None):
+        """Both variants: link rates first, a warm-up step each, then `steps` timed
+        steps each.  Returns the e2e JSON object (staged as the headline)."""
+        spec = self.bs.spec
+        sb = step_bytes(spec)
+        link = self.link_rates()
+        out = {}
+        for name, in_place in (("staged", False), ("in_place", True)):
+            self.run(1, in_place)
+            barrier(dist, self.dev)
+            t = max_over_ranks(self.run(steps, in_place), dist, self.dev)
+            link_in = (self.in_place_bytes + 4 * self.bs.bufs["tables"].numel()) if in_place \
+                else self.h2d_bytes
+            floor = link["floor_ms_per_step"] / 1e3 if not in_place else \
+                self.floor_s(link, link_in, self.d2h_bytes)
+            out[name] = {"value": round(sb * steps / t / 1e9, 2), "unit": UNIT,
+                         "link_gbs": round((link_in + self.d2h_bytes) * steps / t / 1e9, 1),
+                         "ms_per_step": round(t / steps * 1e3, 3), "steps": steps,
+                         "link_in_bytes_per_step": int(link_in),
+                         "link_out_bytes_per_step": int(self.d2h_bytes),
+                         "floor_ms_per_step": round(floor * 1e3, 3),
+                         "frac_of_floor": round(floor / (t / steps), 4)}
+        st = out["staged"]
+        return {"value": st["value"], "unit": UNIT, "h2d_bytes_per_step": int(self.h2d_bytes),
+                "d2h_bytes_per_step": int(self.d2h_bytes), "steps": steps,
+                "ms_per_step": st["ms_per_step"], "link_gbs": st["link_gbs"],
+                "value_meaning": "HBM-algorithmic bytes of the step (as `value`) per second "
+                                 "of the end-to-end step; link_gbs = bytes across the host "
+                                 "link per second",
+                "link": dict(link, frac_of_floor=st["frac_of_floor"]),
+                "in_place": out["in_place"],
+                "path": "per step: pinned host -> device copies of the block tables, full "
+                        "block and miss KV, the step through the C ABI (eager calls), each "
+                        "gathered layer's objects -> pinned host as soon as it exists"
+                        + (" (two host slots, one shared device object layer)"
+                           if self.bs.one_layer else " (all layers in one copy)")
+                        + "; in_place: the slice and merge-scatter read the host full block "
+                          "and miss KV in place (KVL_LAUNCH_HOST_SRC), nothing staged"}
+
+    def close(self):
+        for h in [self.h_hit, self.h_miss] + self.h_obj:
+            h.__del__()
+        self.t_hit = self.t_miss = self.t_obj = self.h_obj = None
+
+
+def measure_host_leg(bs, e2e, dev):
+    """DualPath's host-buffer legs on one GB300 (host buffers in Grace memory, over
+    NVLink-C2C): the merge-scatter of every layer read straight from the pinned host
+    full block into the HBM pool (the final H2D and the paging in one pass), and the
+    gather of every layer's objects straight into pinned host memory; each against the
+    copy engines moving the same bytes.  GB/s across the link."""
     import torch
     import layer_wise_paged_gb300 as kvl
     from layer_wise_paged_gb300.batch import Batch
-
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py: no CUDA device")
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    kvl.build()
-    kvl.lib()
-    spec = bench_spec(args)
-    bufs = workloads.allocate(spec, dev)
-    lay = bufs["layout"]
+    spec, b = bs.spec, bs.bufs
+    if bs.one_layer:
+        raise ValueError("the host legs need a workload whose objects hold every layer")
+    main = torch.cuda.current_stream(dev)
     g = (spec.L, spec.P, spec.B, spec.Rp, spec.n_pool)
-    b = Batch(g, lay.requests, bufs["hit"], bufs["miss"], bufs["objects"], bufs["tables"],
-              bufs["src_tables"])
-    pool = bufs["pool"]
+    b_out = Batch(g, b["layout"].requests, b["hit"], b["miss"], e2e.h_obj[0], b["tables"],
+                  b["src_tables"])
+    e2e.b_host.plan(stream=main)
+    b_out.plan(stream=main)
+    bs.batch.plan(stream=main)
+    L = spec.L
+    in_bytes = (sum(spec.t_hit) + sum(spec.t_miss)) * L * spec.R
+    obj_bytes = b["objects"].numel()
+
+    def timed(fn, reps=3):
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(main)
+            fn()
+            e1.record(main)
+            torch.cuda.synchronize(dev)
+            t = e0.elapsed_time(e1) / 1e3
+            best = t if best is None else min(best, t)
+        return best
+
+    H, D = kvl.KVL_LAUNCH_HOST_SRC, kvl.KVL_LAUNCH_HOST_DST
+    t_fused_in = timed(lambda: e2e.b_host.merge_scatter(0, bs.pool, None, main, layer_count=L, flags=H))
+    t_ce_in = timed(lambda: (b["hit"].copy_(e2e.t_hit, non_blocking=True),
+                             b["miss"].copy_(e2e.t_miss, non_blocking=True)))
+    t_fused_out = timed(lambda: b_out.gather(0, bs.pool, main, layer_count=L, flags=D))
+    t_ce_out = timed(lambda: e2e.t_obj[0].copy_(b["objects"], non_blocking=True))
+    for bt in (e2e.b_host, b_out):
+        check_status(bt, main, "in the host legs")
+    fin, fout = in_bytes / t_fused_in / 1e9, obj_bytes / t_fused_out / 1e9
+    cin, cout = in_bytes / t_ce_in / 1e9, obj_bytes / t_ce_out / 1e9
+    return {"workload": spec.name, "h2d_gbs": round(fin, 1), "d2h_gbs": round(fout, 1),
+            "copy_engine_h2d_gbs": round(cin, 1), "copy_engine_d2h_gbs": round(cout, 1),
+            "frac_of_link": {"h2d": round(fin / cin, 3), "d2h": round(fout / cout, 3)},
+            "link_bytes": {"h2d": int(in_bytes), "d2h": int(obj_bytes)},
+            "legs": "h2d: merge-scatter of all layers in one launch, reading the pinned host "
+                    "full block and miss KV (KVL_LAUNCH_HOST_SRC); d2h: gather of all layers "
+                    "in one launch into pinned host objects (KVL_LAUNCH_HOST_DST); "
+                    "frac_of_link = fused rate / copy-engine rate for the same bytes"}
+
+
+def measure_overlap(bs, dev, gemm=8192, budgets=(4, 8, 16, 32, 64)):
+    """Layer-wise pipeline under an SM budget: layer l's merge-scatter (at most k CTAs,
+    so at most k SMs) on a transfer stream, and a synthetic compute kernel for layer l
+    (a bf16 GEMM standing in for the layer's attention) on a compute stream that waits
+    for layer l's transfer.  Transfers run ahead, so layer l+1's copy overlaps layer
+    l's compute.  Per budget: the transfer alone, the compute alone, the pipeline, the
+    pipeline's slowdown against the compute alone, and Tutti's zero-bubble condition
+    T_transfer <= T_compute (Tutti 阅读笔记, eq. (17))."""
+    import torch
+    spec, b, pool = bs.spec, bs.batch, bs.pool
     main = torch.cuda.current_stream(dev)
     b.plan(stream=main)
-    n = args.gemm
-    A = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
-    Bm = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
-    C = torch.empty(n, n, device=dev, dtype=torch.bfloat16)
+    A = torch.randn(gemm, gemm, device=dev, dtype=torch.bfloat16)
+    Bm = torch.randn(gemm, gemm, device=dev, dtype=torch.bfloat16)
+    C = torch.empty(gemm, gemm, device=dev, dtype=torch.bfloat16)
     xfer, comp = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    budgets = [k for k in (4, 8, 16, 32, 64, sms) if k <= sms]
     L = spec.L
     per_layer = op_bytes(spec)["merge_scatter"]
 
@@ -865,19 +1044,14 @@ def run_overlap(args):
             best = t if best is None else min(best, t)
         return best
 
-    def transfers(k, s):
-        for l in range(L):
-            b.merge_scatter(l, pool, None, s, max_ctas=k)
-
-    def computes(s):
+    def computes():
         for _ in range(L):
-            with torch.cuda.stream(s):
-                torch.matmul(A, Bm, out=C)
+            torch.matmul(A, Bm, out=C)
 
-    t_c = timed(lambda: computes(main)) / L
+    t_c = timed(computes) / L
     rows = []
-    for k in budgets:
-        t_r = timed(lambda: transfers(k, main)) / L
+    for k in [k for k in budgets if k < sms] + [sms]:
+        t_r = timed(lambda: [b.merge_scatter(l, pool, None, main, max_ctas=k) for l in range(L)]) / L
 
         def pipeline():
             xfer.wait_stream(main)
@@ -893,128 +1067,231 @@ def run_overlap(args):
             main.wait_stream(xfer)
             main.wait_stream(comp)
         t_p = timed(pipeline) / L
-        rows.append({"sm_budget": k, "transfer_us_alone": round(t_r * 1e6, 1),
-                     "transfer_gbs_alone": round(per_layer / t_r / 1e9, 1),
-                     "compute_us_alone": round(t_c * 1e6, 1),
-                     "pipeline_us_per_layer": round(t_p * 1e6, 1),
-                     "over_compute_frac": round(max(0.0, (t_p - t_c) / t_p), 4),
-                     "zero_bubble_alone": bool(t_r <= t_c)})
-    code, detail = b.status(main)
-    if code != 0:
-        raise SystemExit(f"bench.py: status {code} detail {detail}")
-    print(json.dumps({"metric": "layer-wise overlap of merge-scatter with compute under an SM budget",
-                      "workload": spec.name, "L": L, "gemm": f"bf16 {n}x{n}x{n} per layer",
-                      "transfer": "kvl_merge_scatter_paged per layer, at most sm_budget CTAs",
-                      "rows": rows}), flush=True)
+        rows.append({"sm_budget": k, "t_transfer_us": round(t_r * 1e6, 1),
+                     "transfer_gbs": round(per_layer / t_r / 1e9, 1),
+                     "t_compute_us": round(t_c * 1e6, 1), "pipeline_us": round(t_p * 1e6, 1),
+                     "gemm_slowdown_pct": round(100.0 * (t_p - t_c) / t_c, 2),
+                     "zero_bubble": bool(t_r <= t_c)})
+    check_status(b, main, "in the overlap measurement")
+    ok = [r for r in rows if r["zero_bubble"]]
+    best = min(ok, key=lambda r: r["sm_budget"]) if ok else None
+    return {"workload": spec.name, "gemm": f"bf16 {gemm}x{gemm}x{gemm} per layer",
+            "transfer": "kvl_merge_scatter_paged per layer, at most sm_budget CTAs",
+            "sm_budget": best["sm_budget"] if best else None,
+            "gemm_slowdown_pct": best["gemm_slowdown_pct"] if best else None,
+            "t_transfer_us": best["t_transfer_us"] if best else None,
+            "t_compute_us": round(t_c * 1e6, 1),
+            "summary": "smallest SM budget whose transfer alone meets the zero-bubble "
+                       "condition, with the pipeline's slowdown against the compute alone",
+            "rows": rows}
+
+
+def run_gpu(args):
+    import torch
+    import layer_wise_paged_gb300 as kvl
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the GPU arm has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    kvl.build()
+    kvl.lib()
+    peak, peak_kind = hbm_peak()
+
+    whole = bench_spec(args)
+    log(f"workload {whole.name}: {step_bytes(whole) / 1e9:.1f} GB per step")
+    part, spec = (None, whole) if world == 1 else rank_part(whole, world, rank)
+    if spec is None:
+        raise SystemExit(f"bench.py: rank {rank} of {world} has no part of {whole.name} "
+                         "(more ranks than requests and layers)")
+    clk = ClockSampler(local, Path(args.clocks_csv) if args.clocks_csv else None)
+    m = measure_step(spec, dev, steps=args.steps, warmup=args.warmup,
+                     serial=args.serial_launches, layers_per_launch=args.layers_per_launch,
+                     eager=args.eager, clocks=clk, dist=dist)
+    bs = m["bs"]
+    log(f"headline step measured: {step_bytes(spec) * args.steps / m['elapsed'] / 1e9:.0f} GB/s")
+    one_layer, n_groups = bs.one_layer, len(bs.groups)
+    sb = step_bytes(spec)
+    total_bytes = sum_over_ranks(float(sb * args.steps), dist, dev)
+    value = total_bytes / m["elapsed"] / 1e9
+    summ = step_summary(spec, m, peak)
+    roofline = roofline_of(spec, m, peak, peak_kind)
+    launches_per_step = kvl.kvl_launches_per_call(0) + n_groups * 4
+
+    e2e = None
+    cpu = None
+    ee = None
+    if not args.no_e2e:
+        try:
+            ee = EndToEnd(bs, dev)
+        except MemoryError as exc:
+            e2e = {"skipped": str(exc)}
+            log(f"end to end skipped: {exc}")
+    if ee is not None:
+        e2e = ee.measure(max(3, min(args.e2e_steps, args.steps)), dist)
+        log(f"end to end measured: {e2e['value']} GB/s, in place {e2e['in_place']['value']} GB/s")
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            # the oracle reads the same host inputs the end-to-end step uploads
+            sample = OracleSample(spec, hit=ee.h_hit.np, miss=ee.h_miss.np)
+            cpu = cpu_baseline(spec, args.cpu_seconds, sample)
+            log(f"cpu baseline measured: {cpu['value']} GB/s on {cpu['cores']} threads")
+            del sample
+        ee.close()
+        del ee
+    elif rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample = OracleSample(spec, hit=bs.bufs["hit"].cpu().numpy(),
+                              miss=bs.bufs["miss"].cpu().numpy())
+        cpu = cpu_baseline(spec, args.cpu_seconds, sample)
+        del sample
+
+    extras = world == 1 and not args.no_extras
+    serial = None
+    if extras and not args.serial_launches:
+        ms = measure_step(spec, dev, steps=steps_for(spec, 2.0, lo=5, hi=args.steps), warmup=3,
+                          serial=True, layers_per_launch=args.layers_per_launch, bs=bs)
+        serial = dict(step_summary(spec, ms, peak),
+                      launches="every launch waits for the one before it (no "
+                               "KVL_LAUNCH_OVERLAP_PREVIOUS)")
+        log(f"serial step measured: {serial['step_gbs']} GB/s")
+        del ms
+    del bs, m["bs"]
+    torch.cuda.empty_cache()
+
+    per_workload, host_leg, overlap = {}, None, None
+    if extras:
+        for name in [n for n in SIDE_WORKLOADS if n != spec.name]:
+            side = workloads.get_spec(name)
+            free = torch.cuda.mem_get_info(dev)[0]
+            need = workloads.footprint_bytes(side, objects_one_layer=workloads.footprint_bytes(side) > 160e9)
+            if need + 24e9 > free:
+                per_workload[name] = {"skipped": f"needs {need / 1e9:.0f} GB, {free / 1e9:.0f} GB free"}
+                continue
+            log(f"{name}: allocating {need / 1e9:.0f} GB")
+            ms = measure_step(side, dev, steps=steps_for(side, 1.0), warmup=3)
+            entry = step_summary(side, ms, peak)
+            log(f"{name}: step {entry['step_gbs']} GB/s")
+            bs2 = ms.pop("bs")
+            mser = measure_step(side, dev, steps=steps_for(side, 1.0), warmup=3, serial=True, bs=bs2)
+            entry["serial"] = {k: v for k, v in step_summary(side, mser, peak).items()
+                               if k in ("step_gbs", "us_per_layer", "step_frac", "frac",
+                                        "dominant", "kernels")}
+            del mser["bs"]
+            if name == PIPELINE_WORKLOAD and not args.no_e2e:
+                bs2.serial = False
+                ee = EndToEnd(bs2, dev)
+                e = ee.measure(steps_for(side, 0.5, lo=5, hi=30))
+                entry["e2e"] = {k: e[k] for k in ("value", "link_gbs", "ms_per_step",
+                                                  "h2d_bytes_per_step", "d2h_bytes_per_step",
+                                                  "link", "in_place")}
+                host_leg = measure_host_leg(bs2, ee, dev)
+                log(f"{name}: host legs {host_leg['h2d_gbs']} / {host_leg['d2h_gbs']} GB/s")
+                overlap = measure_overlap(bs2, dev, gemm=args.gemm)
+                log(f"{name}: overlap measured")
+                ee.close()
+                del ee
+            del bs2
+            per_workload[name] = entry
+            torch.cuda.empty_cache()
+
+    if rank == 0:
+        cfg = describe(whole if world > 1 else spec)
+        cfg.update(layers_per_launch=args.layers_per_launch,
+                   objects="one layer (layer stride 0)" if one_layer else "all layers",
+                   hit_layer_buffers=HIT_RING,
+                   us_per_layer=round(m["elapsed"] / args.steps / spec.L * 1e6, 2),
+                   layers_per_s=round(spec.L * args.steps / m["elapsed"], 1),
+                   launch=m["launch"], kernel_timing=m["kernel_timing"],
+                   launch_overlap="none: every launch waits for the one before it"
+                   if args.serial_launches else
+                   "KVL_LAUNCH_OVERLAP_PREVIOUS on a phase's launches after its first (each "
+                   "may start beside its predecessor, on half of an SM's shared memory), "
+                   "KVL_LAUNCH_SHARE_SMS on the first; gather and scatter-back one launch "
+                   "at a time when all layers share one object layer",
+                   step_bytes=sb, kernels=summ["kernels"], launches_per_step=launches_per_step,
+                   parallelism="1 GPU" if world == 1 else
+                   f"{world} ranks, one batch split ({part.kind} per rank), no data-path exchange",
+                   gpu=torch.cuda.get_device_name(dev), per_workload=per_workload)
+        line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(m["elapsed"] / args.steps * 1e3, 4), "higher_is_better": True,
+                "scaling": "strong", "vs_baseline": None, "dtype": "u8",
+                "data": "synthetic (seeded bf16 KV payload; byte copies)", "config": cfg,
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "serial": serial,
+                "host_leg": host_leg, "overlap": overlap,
+                "gpu_launches": launches_per_step * args.steps * world,
+                "clocks": clk.summary()}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
     return 0
 
 
-def run_host_leg(args):
-    """DualPath's host-buffer legs on one GB300: the full prompt KV held in pinned Grace
-    memory, moved over NVLink-C2C.  Fused: merge-scatter of every layer read straight
-    from the host full block into the HBM pool (the final H2D and the paging in one
-    pass), and gather of every layer's objects straight into host memory.  Against:
-    copy-engine copies of the same bytes followed (or preceded) by the device-only op.
-    Reported as GB/s across the link and as a fraction of the copy engines' rate."""
+def run_overlap(args):
+    """The overlap measurement alone, on --workload, as its own JSON line."""
     import torch
     import layer_wise_paged_gb300 as kvl
-    from layer_wise_paged_gb300.batch import Batch, MappedHost
-
     if not torch.cuda.is_available():
         raise SystemExit("bench.py: no CUDA device")
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     kvl.build()
     kvl.lib()
-    spec = bench_spec(args)
-    bufs = workloads.allocate(spec, dev)
-    lay = bufs["layout"]
-    g = (spec.L, spec.P, spec.B, spec.Rp, spec.n_pool)
-    main = torch.cuda.current_stream(dev)
-    hit_h, miss_h = MappedHost(bufs["hit"].numel()), MappedHost(bufs["miss"].numel())
-    obj_h = MappedHost(bufs["objects"].numel())
-    hit_h.np[:] = bufs["hit"].cpu().numpy()
-    miss_h.np[:] = bufs["miss"].cpu().numpy()
-    b_host = Batch(g, lay.requests, hit_h, miss_h, obj_h, bufs["tables"], bufs["src_tables"])
-    b_dev = Batch(g, lay.requests, bufs["hit"], bufs["miss"], bufs["objects"], bufs["tables"],
-                  bufs["src_tables"])
-    b_host.plan(stream=main)
-    b_dev.plan(stream=main)
-    pool = bufs["pool"]
-    L = spec.L
-    in_bytes = (sum(spec.t_hit) + sum(spec.t_miss)) * L * spec.R
-    obj_bytes = bufs["objects"].numel()
-    tin_h = torch.from_numpy(hit_h.np)  # host views for the copy-engine legs
-    tmiss_h = torch.from_numpy(miss_h.np)
-    tobj_h = torch.from_numpy(obj_h.np)
+    bs = BenchStep(bench_spec(args), dev)
+    print(json.dumps(dict(measure_overlap(bs, dev, gemm=args.gemm),
+                          metric="layer-wise overlap of merge-scatter with compute under an SM "
+                                 "budget")), flush=True)
+    return 0
 
-    def timed(fn, reps=4):
-        best = None
-        for _ in range(reps):
-            torch.cuda.synchronize(dev)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(main)
-            fn()
-            e1.record(main)
-            torch.cuda.synchronize(dev)
-            t = e0.elapsed_time(e1) / 1e3
-            best = t if best is None else min(best, t)
-        return best
 
-    H = kvl.KVL_LAUNCH_HOST_SRC
-    D = kvl.KVL_LAUNCH_HOST_DST
-    t_fused_in = timed(lambda: b_host.merge_scatter(0, pool, None, main, layer_count=L, flags=H))
-    t_ce_in = timed(lambda: (bufs["hit"].copy_(tin_h, non_blocking=True),
-                             bufs["miss"].copy_(tmiss_h, non_blocking=True)))
-    t_dev_merge = timed(lambda: b_dev.merge_scatter(0, pool, None, main, layer_count=L))
-    t_fused_out = timed(lambda: b_host.gather(0, pool, main, layer_count=L, flags=D))
-    t_dev_gather = timed(lambda: b_dev.gather(0, pool, main, layer_count=L))
-    t_ce_out = timed(lambda: tobj_h.copy_(bufs["objects"], non_blocking=True))
-    for bt in (b_host, b_dev):
-        code, detail = bt.status(main)
-        if code != 0:
-            raise SystemExit(f"bench.py: status {code} detail {detail}")
-    ce_in_gbs, ce_out_gbs = in_bytes / t_ce_in / 1e9, obj_bytes / t_ce_out / 1e9
-    print(json.dumps({
-        "metric": "host-buffer legs over NVLink-C2C (GB/s across the link)",
-        "workload": spec.name, "L": L, "link_bytes_in": in_bytes, "link_bytes_out": obj_bytes,
-        "h2d": {"fused_merge_scatter_from_host_gbs": round(in_bytes / t_fused_in / 1e9, 1),
-                "copy_engine_gbs": round(ce_in_gbs, 1),
-                "copy_engine_then_device_merge_scatter_gbs":
-                    round(in_bytes / (t_ce_in + t_dev_merge) / 1e9, 1),
-                "fused_frac_of_copy_engine": round(ce_in_gbs and (in_bytes / t_fused_in / 1e9) / ce_in_gbs, 3)},
-        "d2h": {"fused_gather_to_host_gbs": round(obj_bytes / t_fused_out / 1e9, 1),
-                "copy_engine_gbs": round(ce_out_gbs, 1),
-                "device_gather_then_copy_engine_gbs":
-                    round(obj_bytes / (t_dev_gather + t_ce_out) / 1e9, 1),
-                "fused_frac_of_copy_engine": round((obj_bytes / t_fused_out / 1e9) / ce_out_gbs, 3)},
-        "launches": "one launch of all layers per fused leg"}), flush=True)
+def run_host_leg(args):
+    """The host-buffer legs alone, on --workload, as their own JSON line."""
+    import torch
+    import layer_wise_paged_gb300 as kvl
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    kvl.build()
+    kvl.lib()
+    bs = BenchStep(bench_spec(args), dev)
+    ee = EndToEnd(bs, dev)
+    print(json.dumps(dict(measure_host_leg(bs, ee, dev),
+                          metric="host-buffer legs over NVLink-C2C (GB/s across the link)")),
+          flush=True)
+    ee.close()
     return 0
 
 
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--steps", type=int, default=30)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="kvl", choices=["kvl", "reference"])
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=workloads.NAMES)
     p.add_argument("--layers", type=int, default=0,
                    help="use only the first N layers of the workload (small profiling case)")
+    p.add_argument("--requests", type=int, default=0,
+                   help="use only the first N requests of the workload (small profiling case)")
     p.add_argument("--layers-per-launch", type=int, default=1,
                    help="layers each copy launch covers (1 = the layer-wise pipeline)")
     p.add_argument("--objects", default="layer", choices=["layer", "block"],
                    help="object layout: layer-major, or one file per block (2L objects each)")
     p.add_argument("--overlap", action="store_true",
-                   help="measure the layer-wise pipeline with compute under SM budgets")
-    p.add_argument("--gemm", type=int, default=4096, help="GEMM size of the --overlap compute")
+                   help="only measure the layer-wise pipeline with compute under SM budgets")
+    p.add_argument("--gemm", type=int, default=8192, help="GEMM size of the overlap compute")
     p.add_argument("--host-leg", action="store_true",
-                   help="measure the host-buffer legs over NVLink-C2C")
+                   help="only measure the host-buffer legs over NVLink-C2C")
     p.add_argument("--clocks-csv", default="",
                    help="also write the nvidia-smi clock samples of the timed region here")
-    p.add_argument("--e2e-steps", type=int, default=30)
+    p.add_argument("--e2e-steps", type=int, default=4)
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip the serial step, the other workloads, the host legs and the "
+                        "overlap measurement")
     p.add_argument("--eager", action="store_true",
                    help="launch every call from Python instead of replaying a CUDA graph")
     p.add_argument("--serial-launches", action="store_true",

@@ -101,6 +101,20 @@ def test_static_scratch_plan_finds_the_same_duplicate_on_two_calls():
 
 
 def test_static_scratch_plan_rejects_pools_beyond_its_array():
-    big = kvl.geom(SPEC.L, SPEC.P, SPEC.B, SPEC.Rp, kvl.KVL_STATIC_SCRATCH_POOL_BLOCKS + 1)
-    fake = 1 << 20  # never dereferenced: the size check answers first
-    assert kvl.kvl_batch_plan_static_scratch(big, 1, fake, fake, 1, fake, 1 << 30) == kvl.KVL_EINVAL
+    """The refusal comes from the array's limit, not from another check: the geometry
+    itself is valid (kvl_plan_bytes accepts it), a pool of exactly the limit passes the
+    limit check and is stopped by the next one (a misaligned plan: KVL_EALIGN), and one
+    block more is refused before that check is reached (KVL_EINVAL)."""
+    limit = kvl.KVL_STATIC_SCRATCH_POOL_BLOCKS
+    big = kvl.geom(SPEC.L, SPEC.P, SPEC.B, SPEC.Rp, limit + 1)
+    at = kvl.geom(SPEC.L, SPEC.P, SPEC.B, SPEC.Rp, limit)
+    assert kvl.kvl_plan_bytes(big, 1) != 0 and kvl.kvl_plan_bytes(at, 1) != 0
+    fake = 1 << 20  # never dereferenced: every call below is refused on the host
+    huge = 1 << 40
+    call = kvl.kvl_batch_plan_static_scratch
+    assert call(big, 1, fake, fake, 1, fake, huge) == kvl.KVL_EINVAL
+    assert call(big, 1, fake, fake, 1, fake + 8, huge) == kvl.KVL_EINVAL  # limit first
+    assert call(at, 1, fake, fake, 1, fake + 8, huge) == kvl.KVL_EALIGN   # past the limit
+    # at the limit, a plan one byte short of the bitmap-free plan is refused too
+    need = kvl.kvl_plan_layout(at, 1)[8]
+    assert call(at, 1, fake, fake, 1, fake, need - 1) == kvl.KVL_EINVAL

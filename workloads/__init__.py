@@ -62,6 +62,12 @@ class Spec:
     miss_order: str = "layer"   # "layer" ([L, T_miss, P, Rp]) | "token" ([T_miss, L, P, Rp])
     seed: int = 0
     objects: str = "layer"      # "layer" ([L][P][nblk][B][Rp]) | "block" ([nblk][L][P][B][Rp])
+    # One rank's part of a batch split across GPUs (layer_wise_paged_gb300.shard): its
+    # block tables, renumbered into its own pool, and its full-block tables replace the
+    # recipes above; `part` names the part ("" for a whole batch).
+    given_tables: object = field(default=None, compare=False, repr=False)
+    given_src_tables: object = field(default=None, compare=False, repr=False)
+    part: str = ""
 
     @property
     def R(self) -> int:
@@ -134,6 +140,22 @@ def custom_spec(name="custom", *, L, P, B, Rp, t_hit, t_miss, n_pool=None, value
     return replace(s, n_pool=int(n_pool))
 
 
+def part_spec(spec: Spec, part):
+    """The workload of one rank's part of `spec` (a layer_wise_paged_gb300.shard.Part):
+    its requests and layers, a pool of the blocks it uses, its renumbered tables; None
+    for an idle rank.  The payload is drawn from the workload's seed as for any spec."""
+    if part.kind == "idle":
+        return None
+    idx = list(part.requests)
+    l0, l1 = part.layers
+    return replace(spec, L=l1 - l0, t_hit=tuple(spec.t_hit[i] for i in idx),
+                   t_miss=tuple(spec.t_miss[i] for i in idx),
+                   n_pool=max(1, int(len(part.pool_ids))), given_tables=part.tables,
+                   given_src_tables=part.src_tables,
+                   part=f"rank {part.rank} of {part.world}: {part.kind} "
+                        + (f"{idx[0]}..{idx[-1]}" if part.kind == "requests" else f"layers {l0}..{l1 - 1}"))
+
+
 def block_tables(spec: Spec) -> np.ndarray:
     """Per-request block tables, packed back to back in request order (int32).
 
@@ -142,6 +164,8 @@ def block_tables(spec: Spec) -> np.ndarray:
     """
     nblk = spec.nblk()
     total = int(nblk.sum())
+    if spec.given_tables is not None:
+        return np.ascontiguousarray(spec.given_tables, dtype=np.int32)
     g = _rng(spec.seed + 1)
     if total > spec.n_pool:
         raise ValueError(f"{spec.name}: {total} blocks needed, pool holds {spec.n_pool}")
@@ -171,6 +195,8 @@ def source_tables(spec: Spec):
     """
     if spec.source == "contiguous":
         return None
+    if spec.given_src_tables is not None:
+        return np.ascontiguousarray(spec.given_src_tables, dtype=np.int32)
     g = _rng(spec.seed + 2)
     parts = [g.permutation(int(n)) for n in spec.nsrc()]
     if not parts:
