@@ -288,19 +288,24 @@ def recorded_traffic(kernel: str, workload: str):
 # CPU oracle on a bounded sample (baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def phase_launch_flags(op, i, l0, *, ring, n_launches, shared_objects, serial):
+def phase_launch_flags(op, i, l0, *, ring, n_launches, shared_objects, serial, plan_ready=True):
     """Flags of launch i (first layer l0) of an op's phase of n_launches launches.
 
     A launch may overlap the one before it only when the two touch disjoint bytes:
     never the first launch of a phase (it reads the previous phase's output), never a
     slice launch that reuses a buffer of the hit_layer ring (l0 a multiple of `ring`),
     and no gather or scatter-back launch when all layers share one layer of objects.
-    The launch before a run of overlapping ones leaves them half of each SM."""
-    from layer_wise_paged_gb300 import KVL_LAUNCH_OVERLAP_PREVIOUS, KVL_LAUNCH_SHARE_SMS
+    The launch before a run of overlapping ones leaves them half of each SM.  A launch
+    that waits for its predecessor carries KVL_LAUNCH_PLAN_READY (it prefetches while
+    that one drains), except the step's first launch, which follows the plan's own
+    kernels."""
+    from layer_wise_paged_gb300 import (KVL_LAUNCH_OVERLAP_PREVIOUS, KVL_LAUNCH_PLAN_READY,
+                                        KVL_LAUNCH_SHARE_SMS)
+    ready = KVL_LAUNCH_PLAN_READY if plan_ready and not (op == OPS[0] and i == 0) else 0
     if serial or (shared_objects and op in ("gather", "scatter_back")):
-        return 0
+        return ready
     if i == 0 or (op == "slice" and l0 % ring == 0):
-        return KVL_LAUNCH_SHARE_SMS if n_launches > 1 else 0
+        return (KVL_LAUNCH_SHARE_SMS if n_launches > 1 else 0) | ready
     return KVL_LAUNCH_OVERLAP_PREVIOUS
 
 
@@ -521,10 +526,10 @@ class BenchStep:
     workloads keep one layer of objects (object layer stride 0, each layer's gather
     lands in the same > L2-sized region) to fit in HBM."""
 
-    def __init__(self, spec, dev, layers_per_launch=1, serial=False):
+    def __init__(self, spec, dev, layers_per_launch=1, serial=False, plan_ready=True):
         import torch
         from layer_wise_paged_gb300.batch import Batch
-        self.spec, self.serial = spec, serial
+        self.spec, self.serial, self.plan_ready = spec, serial, plan_ready
         self.one_layer = workloads.footprint_bytes(spec) > 160e9
         self.bufs = workloads.allocate(spec, dev, objects_one_layer=self.one_layer)
         lay = self.bufs["layout"]
@@ -543,7 +548,8 @@ class BenchStep:
     def flags(self, op, i, l0):
         """Launch flags of launch i (first layer l0) of op's phase (phase_launch_flags)."""
         return phase_launch_flags(op, i, l0, ring=self.ring, n_launches=len(self.groups),
-                                  shared_objects=self.one_layer, serial=self.serial)
+                                  shared_objects=self.one_layer, serial=self.serial,
+                                  plan_ready=self.plan_ready)
 
     def phases(self, b, s):
         """(op, [launch thunks]) for each phase of batch b's step on stream s."""
@@ -627,20 +633,21 @@ def per_op_figures(spec, groups, phase_s):
 
 
 def measure_step(spec, dev, *, steps, warmup, serial=False, layers_per_launch=1, eager=False,
-                 clocks=None, dist=None, kernel_reps=KERNEL_REPS, bs=None):
+                 clocks=None, dist=None, kernel_reps=KERNEL_REPS, bs=None, plan_ready=True):
     """`warmup` untimed bench steps of `spec`, then `steps` timed ones (CUDA events on
     the launch stream, max over ranks), each a replay of a CUDA graph of one step (or,
     with `eager`, C-ABI calls from Python).  Per-op launch durations come from events
     around each op's phase of launches: the median of `kernel_reps` replays after the
     timed region (a graph's events hold its last replay), or of the timed steps.
     `bs`: the BenchStep of an earlier measurement of the same workload to reuse (its
-    buffers; `serial` replaces its launch rule), else a new one is allocated.
+    buffers; `serial` and `plan_ready` replace its launch rule), else a new one is
+    allocated.
     Returns a dict with the BenchStep (`bs`), `elapsed` (s), `per_op`, `dom` and how
     the step was launched."""
     import torch
     if bs is None:
         bs = BenchStep(spec, dev, layers_per_launch=layers_per_launch, serial=serial)
-    bs.serial = serial
+    bs.serial, bs.plan_ready = serial, plan_ready
     stream = torch.cuda.current_stream(dev)
     for _ in range(warmup):
         bs.enqueue(bs.batch, stream)
@@ -704,8 +711,10 @@ def measure_step(spec, dev, *, steps, warmup, serial=False, layers_per_launch=1,
 def dominant_kernel(m):
     """The dominant op's kernel name, with the pipeline depth most of its launches ran
     with (3 stages when sharing SMs with a neighbour launch, else 6)."""
+    import layer_wise_paged_gb300 as kvl
     bs, dom = m["bs"], m["dom"]
     shares = bs.flags(dom, 1, bs.groups[1][0]) if len(bs.groups) > 1 else 0
+    shares &= kvl.KVL_LAUNCH_OVERLAP_PREVIOUS | kvl.KVL_LAUNCH_SHARE_SMS
     return f"{KERNEL_NAMES[dom]}<{3 if shares else 6}>"
 
 
@@ -1107,9 +1116,10 @@ def run_gpu(args):
         raise SystemExit(f"bench.py: rank {rank} of {world} has no part of {whole.name} "
                          "(more ranks than requests and layers)")
     clk = ClockSampler(local, Path(args.clocks_csv) if args.clocks_csv else None)
+    ready = not args.no_plan_ready
     m = measure_step(spec, dev, steps=args.steps, warmup=args.warmup,
                      serial=args.serial_launches, layers_per_launch=args.layers_per_launch,
-                     eager=args.eager, clocks=clk, dist=dist)
+                     eager=args.eager, clocks=clk, dist=dist, plan_ready=ready)
     bs = m["bs"]
     log(f"headline step measured: {step_bytes(spec) * args.steps / m['elapsed'] / 1e9:.0f} GB/s")
     one_layer, n_groups = bs.one_layer, len(bs.groups)
@@ -1150,7 +1160,8 @@ def run_gpu(args):
     serial = None
     if extras and not args.serial_launches:
         ms = measure_step(spec, dev, steps=steps_for(spec, 2.0, lo=5, hi=args.steps), warmup=3,
-                          serial=True, layers_per_launch=args.layers_per_launch, bs=bs)
+                          serial=True, layers_per_launch=args.layers_per_launch, bs=bs,
+                          plan_ready=ready)
         serial = dict(step_summary(spec, ms, peak),
                       launches="every launch waits for the one before it (no "
                                "KVL_LAUNCH_OVERLAP_PREVIOUS)")
@@ -1169,14 +1180,21 @@ def run_gpu(args):
                 per_workload[name] = {"skipped": f"needs {need / 1e9:.0f} GB, {free / 1e9:.0f} GB free"}
                 continue
             log(f"{name}: allocating {need / 1e9:.0f} GB")
-            ms = measure_step(side, dev, steps=steps_for(side, 1.0), warmup=3)
+            ms = measure_step(side, dev, steps=steps_for(side, 1.0), warmup=3, plan_ready=ready)
             entry = step_summary(side, ms, peak)
             log(f"{name}: step {entry['step_gbs']} GB/s")
             bs2 = ms.pop("bs")
-            mser = measure_step(side, dev, steps=steps_for(side, 1.0), warmup=3, serial=True, bs=bs2)
-            entry["serial"] = {k: v for k, v in step_summary(side, mser, peak).items()
-                               if k in ("step_gbs", "us_per_layer", "step_frac", "frac",
-                                        "dominant", "kernels")}
+            keep = ("step_gbs", "us_per_layer", "step_frac", "frac", "dominant", "kernels")
+            mser = measure_step(side, dev, steps=steps_for(side, 1.0), warmup=3, serial=True,
+                                bs=bs2, plan_ready=ready)
+            entry["serial"] = {k: v for k, v in step_summary(side, mser, peak).items() if k in keep}
+            if name == PIPELINE_WORKLOAD and ready:
+                # the same lone launches without the prefetch ahead of the wait
+                m0 = measure_step(side, dev, steps=steps_for(side, 1.0), warmup=3, serial=True,
+                                  bs=bs2, plan_ready=False)
+                entry["serial_without_plan_ready"] = {
+                    k: v for k, v in step_summary(side, m0, peak).items() if k in keep}
+                del m0["bs"]
             del mser["bs"]
             if name == PIPELINE_WORKLOAD and not args.no_e2e:
                 bs2.serial = False
@@ -1298,6 +1316,8 @@ def parse_args(argv=None):
                    help="no launch starts before the one before it has finished (no "
                         "KVL_LAUNCH_OVERLAP_PREVIOUS)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-plan-ready", action="store_true",
+                   help="no KVL_LAUNCH_PLAN_READY: launches that wait prefetch nothing first")
     a = p.parse_args(argv)
     if a.warmup < 3:
         p.error("--warmup must be at least 3")

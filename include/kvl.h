@@ -109,8 +109,8 @@ typedef struct kvl_launch {
                          concurrent work (an I/O SM budget, as Tutti 阅读笔记 设计二
                          gives its I/O kernels a fixed SM partition) */
     int32_t flags;    /* 0, or KVL_LAUNCH_HOST_SRC or KVL_LAUNCH_HOST_DST (not both),
-                         optionally OR KVL_LAUNCH_OVERLAP_PREVIOUS and / or
-                         KVL_LAUNCH_SHARE_SMS */
+                         optionally OR KVL_LAUNCH_OVERLAP_PREVIOUS, KVL_LAUNCH_SHARE_SMS
+                         and / or KVL_LAUNCH_PLAN_READY */
 } kvl_launch;
 
 /* The copy's sources (resp. destinations) are pinned host memory mapped into the
@@ -144,6 +144,20 @@ typedef struct kvl_launch {
  * just before a run of overlapping calls; KVL_LAUNCH_OVERLAP_PREVIOUS implies it.  A
  * call that runs alone is faster without it.  The host-memory variants ignore it. */
 #define KVL_LAUNCH_SHARE_SMS 8
+
+/* The caller declares that the plan (and the request array and tables it was built
+ * from) was complete before the kernel enqueued just before this call began: no
+ * kernel that may still run writes it, other than the copy calls' own claim counters
+ * and status word.  True of every copy call of a layer-wise pipeline except the first
+ * one after kvl_batch_plan.  A call that must wait for the kernel before it (no
+ * KVL_LAUNCH_OVERLAP_PREVIOUS) then checks the plan, reads its first work items and
+ * prefetches their source rows into L2 (cp.async.bulk.prefetch) while that kernel
+ * drains, and waits only before its first copy; L2 is the device's point of
+ * coherence, so rows the previous kernel writes are still read as it leaves them.
+ * Results are the same with or without the flag; with a plan that is not complete,
+ * undefined.  Ignored with KVL_LAUNCH_OVERLAP_PREVIOUS and by the host-memory
+ * variants. */
+#define KVL_LAUNCH_PLAN_READY 16
 
 /* One request (device memory: the calls take an array of these in device memory).
  * All strides are in bytes. */

@@ -36,6 +36,7 @@ class kvl_launch(ctypes.Structure):
 
 
 KVL_LAUNCH_HOST_SRC, KVL_LAUNCH_HOST_DST, KVL_LAUNCH_OVERLAP_PREVIOUS, KVL_LAUNCH_SHARE_SMS = 1, 2, 4, 8
+KVL_LAUNCH_PLAN_READY = 16
 
 
 class kvl_geom(ctypes.Structure):

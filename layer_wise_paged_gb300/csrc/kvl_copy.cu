@@ -240,6 +240,13 @@ __device__ __forceinline__ void prefetch_l2(const void *p)
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2: a hint, with
+// the same coherence as prefetch_l2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // 32-bit load through the read-only path; volatile so that it is issued where it
 // stands, ahead of the loads that follow it.
 __device__ __forceinline__ uint32_t ld_nc_u32(const void *p)
@@ -336,12 +343,14 @@ __device__ __forceinline__ T shfl_ptr(T p, int src)
 
 // ---- plan checks and metadata ------------------------------------------------
 
-// A plan is usable when it was built (magic) for this geometry, request array and
-// block tables, fits the caller's buffer with the request count it records, and
-// recorded no error.  The checks keep every later index inside the plan's own
-// arrays (all of them below plan_bytes) and the request array it was sized for.
+// A plan matches a call when it was built (magic) for this geometry, request array
+// and block tables, and fits the caller's buffer with the request count it records;
+// these header fields never change after the plan is built.  The checks keep every
+// later index inside the plan's own arrays (all of them below plan_bytes) and the
+// request array it was sized for.  The plan is usable when it also recorded no error
+// (its status word, which copy calls may write).
 template <int OP>
-__device__ __forceinline__ bool plan_usable(const CopyArgs &a)
+__device__ __forceinline__ bool plan_matches(const CopyArgs &a)
 {
     PlanHeader *h = static_cast<PlanHeader *>(a.plan);
     const int32_t n_req = h->n_req;
@@ -352,7 +361,7 @@ __device__ __forceinline__ bool plan_usable(const CopyArgs &a)
         if (blockIdx.x == 0 && threadIdx.x == 0) record_error(h, KVL_EINVAL, 0);
         return false;
     }
-    return h->status == KVL_OK;
+    return true;
 }
 
 // Field of the item record held one word per lane.
@@ -445,6 +454,47 @@ __device__ __forceinline__ bool item_meta(const CopyArgs &a, PlanHeader *h, cons
     return true;
 }
 
+// Prefetch into L2 the source bytes unit (rec, layer l) will read first, at most
+// `budget` of them; returns the bytes asked for.  Token rows of the slice and
+// merge-scatter (a row's P planes are adjacent in both sources: R bytes), whole
+// plane-blocks of the gather and scatter-back.  Reads only the item record, which the
+// plan resolved from addresses its requests declare.
+template <int OP>
+__device__ __forceinline__ uint32_t prefetch_unit(const CopyArgs &a, uint32_t rec, int64_t l,
+                                                  uint32_t budget, int lane)
+{
+    const int64_t Rp = a.Rp, R = int64_t(a.P) * Rp;
+    if (OP == OP_SLICE || OP == OP_MERGE) {
+        // all fields first, by the whole warp (shuffles), then the lane-divergent loop
+        const int32_t n_hit = int32_t(rec_word(rec, 23));
+        const int32_t n = OP == OP_SLICE ? n_hit : int32_t(rec_word(rec, 24));
+        const uint64_t hit = rec_u64(rec, 0) + uint64_t(l * int64_t(rec_u64(rec, 4)));
+        const uint64_t miss = rec_u64(rec, 6) + uint64_t(l * int64_t(rec_u64(rec, 10)));
+        const int64_t hit_ts = int64_t(rec_u64(rec, 2)), miss_ts = int64_t(rec_u64(rec, 8));
+        const int32_t rows = int32_t(int64_t(n) < int64_t(budget) / R ? int64_t(n) : int64_t(budget) / R);
+        for (int s = lane; s < rows; s += 32) {
+            const uint64_t src = s < n_hit ? hit + uint64_t(s * hit_ts) : miss + uint64_t(s * miss_ts);
+            bulk_prefetch_l2(reinterpret_cast<const void *>(src), uint32_t(R));
+        }
+        return uint32_t(rows * R);
+    }
+    // every field is read here, by the whole warp: the shuffles must not sit inside the
+    // lane-divergent loop below
+    const uint64_t obj = rec_u64(rec, 12);
+    const int64_t obj_ps = int64_t(rec_u64(rec, 14)), obj_ls = int64_t(rec_u64(rec, 16));
+    const int64_t b = int32_t(rec_word(rec, 22));
+    const int64_t blk = int64_t(a.B) * Rp;
+    const int32_t planes = int32_t(int64_t(a.P) < int64_t(budget) / blk ? int64_t(a.P) : int64_t(budget) / blk);
+    if (obj == 0) return budget;  // the copy itself records the missing objects
+    for (int p = lane; p < planes; p += 32) {
+        const uint8_t *src = OP == OP_GATHER
+            ? a.pool + ((l * a.P + p) * a.N + b) * blk
+            : reinterpret_cast<const uint8_t *>(obj + uint64_t(l * obj_ls + p * obj_ps));
+        bulk_prefetch_l2(src, uint32_t(blk));
+    }
+    return uint32_t(planes * blk);
+}
+
 // ---- the pipelined copy --------------------------------------------------------
 
 struct StageInfo {
@@ -486,12 +536,42 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
     __syncwarp();
     // Everything this kernel reads may come from the previous kernel on the stream,
     // unless the caller declared the two independent: then the wait moves to the end,
-    // so this kernel still completes after the previous one.
+    // so this kernel still completes after the previous one.  With a plan the caller
+    // declared complete (KVL_LAUNCH_PLAN_READY), the plan is checked and the first
+    // units' source rows are prefetched into L2 before the wait.
     const bool overlap = (a.flags & KVL_LAUNCH_OVERLAP_PREVIOUS) != 0;
-    if (!overlap) grid_dependency_wait();
-    allow_dependents_launch();
+    const bool early = HOST == 0 && !overlap && (a.flags & KVL_LAUNCH_PLAN_READY) != 0;
+    if (!overlap && !early) grid_dependency_wait();
+    // Dependents are let go only once this kernel has passed its own wait (or, when it
+    // overlaps its predecessor, at once): a later launch that overlaps this one must
+    // not start before the kernels this one waits for have finished.
+    if (!early) allow_dependents_launch();
     const uint32_t rec_first = first_in_cap ? ld_nc_u32(first_rec + lane) : 0u;
-    if (!plan_usable<OP>(a)) {
+    bool usable = plan_matches<OP>(a);
+    if (early) {
+        // The plan was complete before the previous kernel began: a status of OK now
+        // means every item record was written, and the records never change after.
+        const PlanHeader *hh = static_cast<const PlanHeader *>(a.plan);
+        if (usable && hh->status == KVL_OK) {
+            const int64_t n_items = hh->n_items;
+            const int64_t n_units = n_items * a.layer_count;
+            uint32_t budget = uint32_t(kStages) * uint32_t(kStageBytes);
+            // this CTA's two statically placed units, as far as the pipeline holds
+            for (int k = 0; k < 2 && budget > 0; ++k) {
+                const int64_t u = int64_t(blockIdx.x) + int64_t(k) * gridDim.x;
+                if (u >= n_units) break;
+                const int64_t item = u % n_items;
+                const uint32_t rec = u < n_items ? rec_first
+                    : ld_nc_u32(reinterpret_cast<const uint32_t *>(
+                                    plan_base + kRecordsOffset + item * int64_t(sizeof(ItemRec))) + lane);
+                budget -= prefetch_unit<OP>(a, rec, a.layer + u / n_items, budget, lane);
+            }
+        }
+        grid_dependency_wait();
+        allow_dependents_launch();
+    }
+    usable = usable && static_cast<const PlanHeader *>(a.plan)->status == KVL_OK;
+    if (!usable) {
         if (lane == 0)
             for (int s = 0; s < kStages; ++s) mbar_inval(bar0 + 8 * s);
         if (overlap) grid_dependency_wait();
@@ -832,7 +912,8 @@ kvl_status common_checks(const kvl_geom *g, const void *d_plan, size_t plan_byte
     const kvl_status s = check_geom(g);
     if (s) return s;
     constexpr int32_t kHostBoth = KVL_LAUNCH_HOST_SRC | KVL_LAUNCH_HOST_DST;
-    constexpr int32_t kKnown = kHostBoth | KVL_LAUNCH_OVERLAP_PREVIOUS | KVL_LAUNCH_SHARE_SMS;
+    constexpr int32_t kKnown = kHostBoth | KVL_LAUNCH_OVERLAP_PREVIOUS | KVL_LAUNCH_SHARE_SMS |
+                               KVL_LAUNCH_PLAN_READY;
     if (opts && (opts->max_ctas < 0 || (opts->flags & ~kKnown) ||
                  (opts->flags & kHostBoth) == kHostBoth))
         return KVL_EINVAL;

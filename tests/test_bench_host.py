@@ -13,7 +13,7 @@ import bench
 import layer_wise_paged_gb300 as kvl
 import workloads
 
-OV, SH = kvl.KVL_LAUNCH_OVERLAP_PREVIOUS, kvl.KVL_LAUNCH_SHARE_SMS
+OV, SH, RD = kvl.KVL_LAUNCH_OVERLAP_PREVIOUS, kvl.KVL_LAUNCH_SHARE_SMS, kvl.KVL_LAUNCH_PLAN_READY
 
 
 def test_llama_layer_bytes_follow_the_kv_size_formula():
@@ -41,9 +41,10 @@ def test_op_bytes_match_the_spec(name):
     assert b["gather"] == 2 * spec.P * int(spec.nblk().sum()) * spec.B * spec.Rp
 
 
-def _flags(op, n, *, ring=8, shared=False, serial=False, K=1):
+def _flags(op, n, *, ring=8, shared=False, serial=False, K=1, ready=False):
     return [bench.phase_launch_flags(op, i, i * K, ring=ring, n_launches=n,
-                                     shared_objects=shared, serial=serial) for i in range(n)]
+                                     shared_objects=shared, serial=serial, plan_ready=ready)
+            for i in range(n)]
 
 
 def test_first_launch_of_a_phase_never_overlaps():
@@ -72,6 +73,19 @@ def test_serial_and_single_launch_phases_carry_no_flags():
     for op in bench.OPS:
         assert _flags(op, 32, serial=True) == [0] * 32
         assert _flags(op, 1) == [0]
+
+
+def test_plan_ready_goes_on_every_waiting_launch_but_the_first_after_the_plan():
+    # the step's first launch (the slice of layer 0) follows the plan's kernels
+    f = _flags("slice", 32, ready=True)
+    assert f[0] == SH and all(x & RD for x in f[8::8]) and all(x == OV for x in f[1:8])
+    for op in bench.OPS[1:]:
+        g = _flags(op, 32, ready=True)
+        assert g[0] == SH | RD and g[1:] == [OV] * 31  # an overlapping launch needs no prefetch
+    assert _flags("gather", 4, shared=True, ready=True) == [RD] * 4
+    assert _flags("merge_scatter", 3, serial=True, ready=True) == [RD] * 3
+    assert _flags("slice", 3, serial=True, ready=True) == [0, RD, RD]
+    assert _flags("merge_scatter", 3, serial=True) == [0] * 3
 
 
 def test_traffic_record_is_read_only_for_the_current_kernel_source():

@@ -176,7 +176,7 @@ def test_host_side_checks_return_without_launching():
                                        s) == kvl.KVL_EINVAL
     assert kvl.kvl_merge_scatter_paged(g, plan, pb, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 7),
                                        s) == kvl.KVL_EINVAL
-    assert kvl.kvl_merge_scatter_paged(g, plan, pb, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 16),
+    assert kvl.kvl_merge_scatter_paged(g, plan, pb, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 64),
                                        s) == kvl.KVL_EINVAL
     assert kvl.kvl_merge_scatter_paged(g, plan, pb, reqs, tabs, 0, 1, pool, None, kvl.kvl_launch(0, 11),
                                        s) == kvl.KVL_EINVAL

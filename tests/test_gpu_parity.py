@@ -477,13 +477,55 @@ def test_gather_writes_host_objects_and_scatter_back_reads_them():
     assert gb.status() == (0, 0)
 
 
+@pytest.mark.parametrize("rows", [2048, 1152])
+def test_plan_ready_launches_read_what_the_kernel_before_them_writes(rows):
+    """Every launch after the first carries KVL_LAUNCH_PLAN_READY and reads what the
+    launch just before it writes: merge-scatter of layer l, then the gather of that
+    layer's blocks, then their scatter-back into a second pool, layer after layer, with
+    the slice of the next layer between (a lone launch of another op).  Each waiting
+    launch prefetches its first rows into L2 while its predecessor still writes them;
+    the results must still be the oracle's, byte for byte."""
+    import layer_wise_paged_gb300 as kvl
+    spec = workloads.custom_spec(L=4, P=2 if rows == 2048 else 1, B=16, Rp=rows,
+                                 t_hit=[2100, 700, 1500], t_miss=[90, 400, 33],
+                                 table="fragmented", source="permuted", seed=8801 + rows)
+    hb = host_buffers(spec)
+    gb, d = device_batch(spec, hb)
+    ob = oracle_batch(spec, hb)
+    gb.plan()
+    R, L = spec.R, spec.L
+    n_hit = ob.total_hit() * R
+    hit_out = sentinel_dev(L * n_hit)
+    pool2 = torch.full_like(d.pool, SENT)
+    ready = kvl.KVL_LAUNCH_PLAN_READY
+    for layer in range(L):
+        gb.slice_layer(layer, hit_out[layer * n_hit:], flags=ready if layer else 0)
+        gb.merge_scatter(layer, d.pool, flags=ready)
+        gb.gather(layer, d.pool, flags=ready)
+        gb.scatter_back(layer, pool2, flags=ready, max_ctas=[None, 7][layer % 2])
+    want_hit = np.full(L * n_hit + GUARD, SENT, np.uint8)
+    pool2_h = np.full_like(hb.pool, SENT)
+    for layer in range(L):
+        want_hit[layer * n_hit:(layer + 1) * n_hit] = ob.slice_layer(layer)[1]
+        assert ob.merge_scatter(layer, hb.pool)[0] == 0
+        assert ob.gather_objects(layer, hb.pool) == 0
+        assert ob.scatter_back(layer, pool2_h) == 0
+    assert_bytes_equal(hit_out, want_hit, "hit_out")
+    assert_bytes_equal(d.pool, hb.pool, "pool")
+    assert_bytes_equal(d.objects, hb.objects, "objects")
+    assert_bytes_equal(pool2, pool2_h, "second pool")
+    assert gb.status() == (0, 0)
+
+
 @pytest.mark.parametrize("case", range(46))
 def test_random_launch_plans_equal_the_oracle(case):
     """Random ragged batches under random launch plans: per op, random layers per
     launch, SM budgets and overlap flags (every launch of a phase after the first may
-    overlap its predecessor; the first shares SMs or not).  Budgets as small as one
-    CTA let long chains of launches run at once.  Cases 30 and up draw batches large
-    enough for tensor maps."""
+    overlap its predecessor; the first shares SMs or not), and KVL_LAUNCH_PLAN_READY on
+    any launch but the first after the plan (a phase's first launch then prefetches the
+    rows the phase before it is still writing).  Budgets as small as one CTA let long
+    chains of launches run at once.  Cases 30 and up draw batches large enough for
+    tensor maps."""
     import layer_wise_paged_gb300 as kvl
     if case >= 30:
         g, spec = _mapped_spec(97000 + case)
@@ -507,7 +549,7 @@ def test_random_launch_plans_equal_the_oracle(case):
     hit_out = sentinel_dev(L * n_hit)
     complete = sentinel_dev(L * n_tok)
 
-    def plan_of_launches():
+    def plan_of_launches(after_plan=False):
         K = int(g.integers(1, L + 1))
         out = []
         for i, l0 in enumerate(range(0, L, K)):
@@ -516,11 +558,13 @@ def test_random_launch_plans_equal_the_oracle(case):
                 f = kvl.KVL_LAUNCH_SHARE_SMS
             elif i > 0 and g.random() < 0.8:
                 f = kvl.KVL_LAUNCH_OVERLAP_PREVIOUS
+            if not (after_plan and i == 0) and g.random() < 0.7:
+                f |= kvl.KVL_LAUNCH_PLAN_READY
             out.append((l0, min(K, L - l0), dict(max_ctas=[None, 1, 5, 40][int(g.integers(0, 4))],
                                                   flags=f)))
         return out
 
-    for l0, k, o in plan_of_launches():
+    for l0, k, o in plan_of_launches(after_plan=True):
         gb.slice_layer(l0, hit_out[l0 * n_hit:], layer_count=k, **o)
     for l0, k, o in plan_of_launches():
         gb.merge_scatter(l0, d.pool, complete[l0 * n_tok:], layer_count=k, **o)
