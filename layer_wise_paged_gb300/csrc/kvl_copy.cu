@@ -548,12 +548,31 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
     if (!early) allow_dependents_launch();
     const uint32_t rec_first = first_in_cap ? ld_nc_u32(first_rec + lane) : 0u;
     bool usable = plan_matches<OP>(a);
+    // The header fields below never change once the plan is built.  A launch with a
+    // complete plan (early) reads them, and acquires the tensor maps its first unit
+    // reads through, before its dependency wait, so that after the wait only the
+    // status word stands between it and its first load.
+    PlanHeader *h = static_cast<PlanHeader *>(a.plan);
+    PlanView v;
+    int64_t n_items = 0, n_hit_all = 0, n_tok_all = 0;
+    int32_t map_chunk = 0;
+    constexpr bool kMaps = HOST == 0 && (OP == OP_SLICE || OP == OP_MERGE);
+    auto read_header = [&]() {
+        v = plan_view(a.plan, h->n_req, h->pool_blocks, h->n_layers);
+        n_items = h->n_items;
+        n_hit_all = h->n_hit;
+        n_tok_all = h->n_tokens;
+        map_chunk = kMaps ? h->map_chunk : 0;
+    };
+    // lane 0's four most recently acquired maps, newest first
+    const uint8_t *acq0 = nullptr, *acq1 = nullptr, *acq2 = nullptr, *acq3 = nullptr;
+    bool header_read = false;
     if (early) {
         // The plan was complete before the previous kernel began: a status of OK now
         // means every item record was written, and the records never change after.
-        const PlanHeader *hh = static_cast<const PlanHeader *>(a.plan);
-        if (usable && hh->status == KVL_OK) {
-            const int64_t n_items = hh->n_items;
+        if (usable && h->status == KVL_OK) {
+            read_header();
+            header_read = true;
             const int64_t n_units = n_items * a.layer_count;
             uint32_t budget = uint32_t(kStages) * uint32_t(kStageBytes);
             // this CTA's two statically placed units, as far as the pipeline holds
@@ -566,20 +585,40 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
                                     plan_base + kRecordsOffset + item * int64_t(sizeof(ItemRec))) + lane);
                 budget -= prefetch_unit<OP>(a, rec, a.layer + u / n_items, budget, lane);
             }
+            // the tensor maps of the first unit's request that this op reads through
+            // (at most four: a kind and its tail kind for each of two sources)
+            if (kMaps && map_chunk > 0 && int64_t(blockIdx.x) < n_items) {
+                const int32_t flags = int32_t(rec_word(rec_first, 29));
+                const uint8_t *req_maps = v.maps + int64_t(int32_t(rec_word(rec_first, 25))) *
+                                                       (kMapsPerReq * kMapBytes);
+                if (lane == 0) {
+                    const int kinds[4] = {OP == OP_SLICE ? MAP_SLICE : MAP_HIT,
+                                          (OP == OP_SLICE ? MAP_SLICE : MAP_HIT) + kMapTail,
+                                          OP == OP_SLICE ? -1 : MAP_MISS,
+                                          OP == OP_SLICE ? -1 : MAP_MISS + kMapTail};
+                    for (int i = 0; i < 4; ++i) {
+                        if (kinds[i] < 0 || !(flags & map_bit(kinds[i]))) continue;
+                        const uint8_t *m = req_maps + kinds[i] * kMapBytes;
+                        acquire_tensor_map(m);
+                        acq3 = acq2;
+                        acq2 = acq1;
+                        acq1 = acq0;
+                        acq0 = m;
+                    }
+                }
+            }
         }
         grid_dependency_wait();
         allow_dependents_launch();
     }
-    usable = usable && static_cast<const PlanHeader *>(a.plan)->status == KVL_OK;
+    usable = usable && h->status == KVL_OK;
     if (!usable) {
         if (lane == 0)
             for (int s = 0; s < kStages; ++s) mbar_inval(bar0 + 8 * s);
         if (overlap) grid_dependency_wait();
         return;
     }
-    PlanHeader *h = static_cast<PlanHeader *>(a.plan);
-    const PlanView v = plan_view(a.plan, h->n_req, h->pool_blocks, h->n_layers);
-    const int64_t n_items = h->n_items;
+    if (!header_read) read_header();
     ClaimCounter *ctr = &v.counters[int64_t(a.layer) * kOps + OP];
     const int64_t G = gridDim.x;
 
@@ -589,14 +628,10 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
     const int64_t R = int64_t(a.P) * a.Rp;
     // Tensor maps (device buffers only): a segment of box_rows rows from one source
     // that has a map is one tensor load; plane p starts at chunk p * Rp / chunk.
-    constexpr bool kMaps = HOST == 0 && (OP == OP_SLICE || OP == OP_MERGE);
-    const int32_t map_chunk = kMaps ? h->map_chunk : 0;
     const uint8_t *maps = map_chunk > 0 ? v.maps : nullptr;
     const int box_rows = segment_rows(a.B, row_bytes);        // a whole segment's box
     const int tail_rows = segment_tail_rows(a.B, row_bytes);  // a block tail's box (0: none)
     const int32_t plane_chunks = map_chunk > 0 ? a.Rp / map_chunk : 0;
-    // lane 0's four most recently acquired maps, newest first
-    const uint8_t *acq0 = nullptr, *acq1 = nullptr, *acq2 = nullptr, *acq3 = nullptr;
 
     int64_t issued = 0, retired = 0;
     bool timed_out = false;
@@ -657,7 +692,6 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
     auto layer_of = [&](int64_t u) -> int64_t {
         return int64_t(a.layer) + (one_layer ? 0 : int64_t(uint32_t(u) / n_items32));
     };
-    const int64_t n_hit_all = h->n_hit, n_tok_all = h->n_tokens;
     int64_t cur = blockIdx.x;
     const int64_t nxt_static = blockIdx.x + G;
     // unit cur < n_items is item cur of the first layer: the record read above

@@ -137,6 +137,32 @@ def test_missing_objects_pointer_is_einval_at_gather():
     assert gb.status() == (kvl.KVL_EINVAL, 0)
 
 
+def test_a_plan_that_fails_while_a_plan_ready_launch_waits_writes_nothing():
+    """A launch with KVL_LAUNCH_PLAN_READY checks the plan before its dependency wait and
+    reads the status word again after it.  Here the gather before it records
+    KVL_EINVAL late in its run (the request without objects is the last one claimed),
+    so the merge-scatter after it may find the plan sound before the wait and failed
+    after it: either way it must write nothing to its (sentinel) pool."""
+    spec = workloads.custom_spec(L=2, P=2, B=16, Rp=2048, t_hit=[12000, 9000, 20],
+                                 t_miss=[300, 100, 4], table="perm", seed=31)
+    hb = host_buffers(spec)
+    gb, d = device_batch(spec, hb)
+    host = kvl.pack_requests(hb.layout.requests, hit_base=d.hit.data_ptr(),
+                             miss_base=d.miss.data_ptr(), obj_base=d.objects.data_ptr())
+    host[2]["objects"] = 0  # the last request has no objects: its gather item fails
+    gb.d_reqs.copy_(torch.from_numpy(host.view(np.uint8).reshape(-1).copy()))
+    pool2 = torch.full_like(d.pool, workloads.SENTINEL)
+    for rep in range(3):
+        gb.plan()
+        gb.merge_scatter(0, d.pool)
+        assert gb.status() == (0, 0)
+        gb.gather(0, d.pool)
+        gb.merge_scatter(1, pool2, flags=kvl.KVL_LAUNCH_PLAN_READY)
+        gb.gather(1, d.pool, flags=kvl.KVL_LAUNCH_PLAN_READY)
+        assert gb.status() == (kvl.KVL_EINVAL, 2), rep
+        assert bool((pool2 == workloads.SENTINEL).all()), f"repetition {rep}: a failed plan wrote"
+
+
 def test_host_side_checks_return_without_launching():
     hb = host_buffers(SPEC)
     gb, d = device_batch(SPEC, hb)
