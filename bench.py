@@ -767,11 +767,13 @@ class EndToEnd:
 
     Launches are eager C-ABI calls from Python.  Copies run on their own streams: a
     step's uploads start once the previous step's merge-scatter no longer reads the
-    inputs, and each layer's read-back overlaps the next layer's gather where the
-    objects buffer allows (one shared object layer: a gather waits for the previous
-    layer's read-back)."""
+    inputs.  When all layers share one object layer (the largest workloads), the
+    gathers rotate over a ring of `ring` device object layers, each with its own
+    batch and plan: a layer's gather waits only for the read-back of the layer that
+    last used its slot, so read-backs run behind the next layers' gathers and the next
+    step's slice and merge-scatter.  Scatter-back of layer l reads slot l mod ring."""
 
-    def __init__(self, bs, dev):
+    def __init__(self, bs, dev, ring=4):
         import torch
         from layer_wise_paged_gb300.batch import Batch, MappedHost
         self.bs, self.dev = bs, dev
@@ -798,32 +800,42 @@ class EndToEnd:
         self.t_obj = [torch.from_numpy(h.np)[:n_obj] for h in self.h_obj]
         spec, lay = bs.spec, b["layout"]
         g = (spec.L, spec.P, spec.B, spec.Rp, spec.n_pool)
-        # the in-place batch: the same requests, their hit and miss rows at the mapped
+        # the object slots: the bench's own objects buffer, and for a shared object layer
+        # ring - 1 more of the same size, each with a batch (and plan) of its own
+        self.ring = max(1, min(int(ring), spec.L)) if bs.one_layer else 1
+        self.d_obj = [b["objects"]] + [torch.full_like(b["objects"], workloads.SENTINEL)
+                                       for _ in range(self.ring - 1)]
+        self.b_dev = [bs.batch] + [Batch(g, lay.requests, b["hit"], b["miss"], o, b["tables"],
+                                         b["src_tables"]) for o in self.d_obj[1:]]
+        # the in-place batches: the same requests, their hit and miss rows at the mapped
         # host addresses
-        self.b_host = Batch(g, lay.requests, self.h_hit, self.h_miss, b["objects"], b["tables"],
-                            b["src_tables"])
+        self.b_hosts = [Batch(g, lay.requests, self.h_hit, self.h_miss, o, b["tables"],
+                              b["src_tables"]) for o in self.d_obj]
+        self.b_host = self.b_hosts[0]
         self.main = torch.cuda.current_stream(dev)
         self.h2d, self.d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        self.ev_in, self.ev_free, self.ev_g, self.ev_out = (torch.cuda.Event() for _ in range(4))
+        self.ev_in, self.ev_free, self.ev_g = (torch.cuda.Event() for _ in range(3))
+        self.ev_slot = [torch.cuda.Event() for _ in range(self.ring)]  # slot read back
         self.h2d_bytes = b["hit"].numel() + b["miss"].numel() + 4 * b["tables"].numel()
         self.reads_back = spec.L if bs.one_layer else 1
         self.d2h_bytes = n_obj * self.reads_back
         # bytes the in-place slice and merge-scatter read across the link per step
         self.in_place_bytes = (op_bytes(spec)["slice"] + op_bytes(spec)["merge_scatter"]) // 2 * spec.L
 
-    def _read_back(self, slot):
+    def _read_back(self, slot, host_slot):
         import torch
         self.ev_g.record(self.main)
         self.d2h.wait_event(self.ev_g)
         with torch.cuda.stream(self.d2h):
-            self.t_obj[slot].copy_(self.bs.bufs["objects"], non_blocking=True)
-        self.ev_out.record(self.d2h)
+            self.t_obj[host_slot].copy_(self.d_obj[slot], non_blocking=True)
+        self.ev_slot[slot].record(self.d2h)
 
     def _step(self, in_place):
         import torch
         import layer_wise_paged_gb300 as kvl
         bs, s, b = self.bs, self.main, self.bs.bufs
-        batch = self.b_host if in_place else bs.batch
+        batches = self.b_hosts if in_place else self.b_dev
+        batch = batches[0]
         # inputs: uploaded once the previous step's merge-scatter no longer reads them
         self.h2d.wait_event(self.ev_free)
         with torch.cuda.stream(self.h2d):
@@ -833,7 +845,8 @@ class EndToEnd:
                 b["miss"].copy_(self.t_miss, non_blocking=True)
         self.ev_in.record(self.h2d)
         s.wait_event(self.ev_in)
-        batch.plan(stream=s)
+        for bt in batches:
+            bt.plan(stream=s)
         host = kvl.KVL_LAUNCH_HOST_SRC
         for i, (l0, n) in enumerate(bs.groups):
             batch.slice_layer(l0, bs.hit_views[l0], s, layer_count=n,
@@ -843,15 +856,17 @@ class EndToEnd:
                                 flags=host if in_place else bs.flags("merge_scatter", i, l0))
         self.ev_free.record(s)
         for i, (l0, n) in enumerate(bs.groups):
+            k = i % self.ring
             if bs.one_layer or i == 0:
-                s.wait_event(self.ev_out)  # the objects buffer has been read back
-            batch.gather(l0, bs.pool, s, layer_count=n, flags=bs.flags("gather", i, l0))
+                s.wait_event(self.ev_slot[k])  # the slot's last objects have been read back
+            batches[k].gather(l0, bs.pool, s, layer_count=n, flags=bs.flags("gather", i, l0))
             if bs.one_layer:
-                self._read_back(i % 2)
+                self._read_back(k, i % 2)
         if not bs.one_layer:
-            self._read_back(0)
+            self._read_back(0, 0)
         for i, (l0, n) in enumerate(bs.groups):
-            batch.scatter_back(l0, bs.pool, s, layer_count=n, flags=bs.flags("scatter_back", i, l0))
+            batches[i % self.ring].scatter_back(l0, bs.pool, s, layer_count=n,
+                                                flags=bs.flags("scatter_back", i, l0))
 
     def run(self, n, in_place):
         """n steps; returns seconds (CUDA events on the launch stream)."""
@@ -860,15 +875,16 @@ class EndToEnd:
         torch.cuda.synchronize(self.dev)
         e0.record(self.main)
         self.ev_free.record(self.main)
-        self.ev_out.record(self.main)
+        for ev in self.ev_slot:
+            ev.record(self.main)
         for _ in range(n):
             self._step(in_place)
         self.main.wait_stream(self.h2d)
         self.main.wait_stream(self.d2h)
         e1.record(self.main)
         torch.cuda.synchronize(self.dev)
-        check_status(self.b_host if in_place else self.bs.batch, self.main,
-                     "in the end-to-end steps")
+        for bt in (self.b_hosts if in_place else self.b_dev):
+            check_status(bt, self.main, "in the end-to-end steps")
         return e0.elapsed_time(e1) / 1e3
 
     def link_rates(self, reps=2):
@@ -903,7 +919,8 @@ class EndToEnd:
         def down():
             with torch.cuda.stream(self.d2h):
                 for k in range(self.reads_back):
-                    self.t_obj[k % len(self.t_obj)].copy_(b["objects"], non_blocking=True)
+                    self.t_obj[k % len(self.t_obj)].copy_(self.d_obj[k % self.ring],
+                                                          non_blocking=True)
 
         t_up, t_down = timed(up), timed(down)
         t_both = timed(lambda: (up(), down()))
@@ -953,8 +970,8 @@ class EndToEnd:
                 "path": "per step: pinned host -> device copies of the block tables, full "
                         "block and miss KV, the step through the C ABI (eager calls), each "
                         "gathered layer's objects -> pinned host as soon as it exists"
-                        + (" (two host slots, one shared device object layer)"
-                           if self.bs.one_layer else " (all layers in one copy)")
+                        + (f" (a ring of {self.ring} device object layers, one plan each, "
+                           "two host slots)" if self.bs.one_layer else " (all layers in one copy)")
                         + "; in_place: the slice and merge-scatter read the host full block "
                           "and miss KV in place (KVL_LAUNCH_HOST_SRC), nothing staged"}
 
@@ -962,6 +979,7 @@ class EndToEnd:
         for h in [self.h_hit, self.h_miss] + self.h_obj:
             h.__del__()
         self.t_hit = self.t_miss = self.t_obj = self.h_obj = None
+        self.d_obj = self.b_dev = self.b_hosts = self.b_host = None
 
 
 def measure_host_leg(bs, e2e, dev):
