@@ -33,11 +33,14 @@
 // wait is bounded by the global timer: past the limit the kernel records
 // KVL_ETIMEOUT, waits (bounded again) for its copies in flight and returns.
 //
-// Ordering between launches: programmatic dependent launch.  A kernel lets its
-// successor launch as soon as it starts, and waits for its predecessor
-// (griddepcontrol.wait) before its first read, or, when the caller declared the two
-// independent (KVL_LAUNCH_OVERLAP_PREVIOUS), just before it exits, so it still
-// completes after its predecessor.
+// Ordering between launches: programmatic dependent launch.  A kernel waits for its
+// predecessor (griddepcontrol.wait) before its first read and then lets its successor
+// launch; or, when the caller declared the two independent
+// (KVL_LAUNCH_OVERLAP_PREVIOUS), it lets its successor launch at once and waits just
+// before it exits, so it still completes after its predecessor.  With a plan the
+// caller declared complete (KVL_LAUNCH_PLAN_READY), a waiting kernel checks the plan,
+// reads its first records, acquires its first tensor maps and prefetches its first
+// source rows into L2 (cp.async.bulk.prefetch) before the wait.
 #include <cstdint>
 
 #include "kvl_internal.cuh"
