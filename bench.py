@@ -765,22 +765,25 @@ class EndToEnd:
       and the miss KV straight from pinned host memory (KVL_LAUNCH_HOST_SRC: SM loads
       over the link), so nothing is staged in HBM first.
 
-    Launches are eager C-ABI calls from Python.  Copies run on their own streams: a
-    step's uploads start once the previous step's merge-scatter no longer reads the
-    inputs.  When all layers share one object layer (the largest workloads), the
-    gathers rotate over a ring of `ring` device object layers, each with its own
-    batch and plan: a layer's gather waits only for the read-back of the layer that
-    last used its slot, so read-backs run behind the next layers' gathers and the next
-    step's slice and merge-scatter.  Scatter-back of layer l reads slot l mod ring."""
+    Launches are eager C-ABI calls from Python; copies run on their own streams.
+    Where device memory allows, the staged step alternates two device input sets: a
+    step's uploads go to the set the step before last used, once that step's
+    merge-scatter is done with it, so they run while the previous step still slices
+    and merges.  Object buffers are slots that a gather waits on only until the slot's
+    last read-back is done.  With all layers in one object buffer, each input set has
+    its own.  When all layers share one object layer (the largest workloads), the
+    gathers rotate over a ring of `ring` such layers, so read-backs trail the gathers;
+    scatter-back of layer l then reads slot l mod ring.  Each (input set, slot) pair
+    has its own batch and plan."""
 
-    def __init__(self, bs, dev, ring=4):
+    def __init__(self, bs, dev, ring=4, two_sets=True):
         import torch
         from layer_wise_paged_gb300.batch import Batch, MappedHost
         self.bs, self.dev = bs, dev
         b = bs.bufs
         n_obj = b["objects"].numel()
-        slots = 2 if bs.one_layer else 1
-        need = b["hit"].numel() + b["miss"].numel() + slots * n_obj
+        host_slots = 2 if bs.one_layer else 1
+        need = b["hit"].numel() + b["miss"].numel() + host_slots * n_obj
         avail = host_available()
         if need > 0.6 * avail:
             raise MemoryError(f"pinned host buffers of {need / 1e9:.0f} GB, host memory "
@@ -788,7 +791,7 @@ class EndToEnd:
         log(f"end to end: pinning {need / 1e9:.1f} GB of host memory")
         self.h_hit = MappedHost(b["hit"].numel())
         self.h_miss = MappedHost(b["miss"].numel())
-        self.h_obj = [MappedHost(n_obj) for _ in range(slots)]
+        self.h_obj = [MappedHost(n_obj) for _ in range(host_slots)]
         log("end to end: host buffers pinned")
         self.t_hit = torch.from_numpy(self.h_hit.np)[:b["hit"].numel()]
         self.t_miss = torch.from_numpy(self.h_miss.np)[:b["miss"].numel()]
@@ -800,22 +803,32 @@ class EndToEnd:
         self.t_obj = [torch.from_numpy(h.np)[:n_obj] for h in self.h_obj]
         spec, lay = bs.spec, b["layout"]
         g = (spec.L, spec.P, spec.B, spec.Rp, spec.n_pool)
-        # the object slots: the bench's own objects buffer, and for a shared object layer
-        # ring - 1 more of the same size, each with a batch (and plan) of its own
-        self.ring = max(1, min(int(ring), spec.L)) if bs.one_layer else 1
+        # device input sets: the bench's own, and a second one where memory allows
+        second = b["hit"].numel() + b["miss"].numel() + (0 if bs.one_layer else n_obj)
+        self.n_sets = 2 if two_sets and second + 16e9 < torch.cuda.mem_get_info(dev)[0] else 1
+        self.sets = [dict(hit=b["hit"], miss=b["miss"], tables=b["tables"])]
+        if self.n_sets == 2:
+            self.sets.append(dict(hit=torch.empty_like(b["hit"]), miss=torch.empty_like(b["miss"]),
+                                  tables=torch.empty_like(b["tables"])))
+        # object slots: a ring of shared object layers, or one buffer per input set
+        self.ring = max(1, min(int(ring), spec.L)) if bs.one_layer else self.n_sets
         self.d_obj = [b["objects"]] + [torch.full_like(b["objects"], workloads.SENTINEL)
                                        for _ in range(self.ring - 1)]
-        self.b_dev = [bs.batch] + [Batch(g, lay.requests, b["hit"], b["miss"], o, b["tables"],
-                                         b["src_tables"]) for o in self.d_obj[1:]]
-        # the in-place batches: the same requests, their hit and miss rows at the mapped
-        # host addresses
+        # batches: staged [set][slot], in place [slot] (their inputs are the host's)
+        self.b_dev = [[bs.batch if (si, k) == (0, 0) else
+                       Batch(g, lay.requests, st["hit"], st["miss"], o, st["tables"], b["src_tables"])
+                       for k, o in enumerate(self.d_obj)] for si, st in enumerate(self.sets)]
         self.b_hosts = [Batch(g, lay.requests, self.h_hit, self.h_miss, o, b["tables"],
                               b["src_tables"]) for o in self.d_obj]
         self.b_host = self.b_hosts[0]
         self.main = torch.cuda.current_stream(dev)
         self.h2d, self.d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        self.ev_in, self.ev_free, self.ev_g = (torch.cuda.Event() for _ in range(3))
-        self.ev_slot = [torch.cuda.Event() for _ in range(self.ring)]  # slot read back
+        self.ev_g = torch.cuda.Event()
+        self.ev_in = [torch.cuda.Event() for _ in range(self.n_sets)]
+        self.ev_free = [torch.cuda.Event() for _ in range(self.n_sets)]  # set's inputs done with
+        self.ev_slot = [torch.cuda.Event() for _ in range(self.ring)]    # slot read back
+        self.n_step = 0
+        self.used = set()  # the batches steps have planned and used (their status is read)
         self.h2d_bytes = b["hit"].numel() + b["miss"].numel() + 4 * b["tables"].numel()
         self.reads_back = spec.L if bs.one_layer else 1
         self.d2h_bytes = n_obj * self.reads_back
@@ -833,20 +846,30 @@ class EndToEnd:
     def _step(self, in_place):
         import torch
         import layer_wise_paged_gb300 as kvl
-        bs, s, b = self.bs, self.main, self.bs.bufs
-        batches = self.b_hosts if in_place else self.b_dev
-        batch = batches[0]
-        # inputs: uploaded once the previous step's merge-scatter no longer reads them
-        self.h2d.wait_event(self.ev_free)
+        bs, s = self.bs, self.main
+        si = 0 if in_place else self.n_step % self.n_sets
+        self.n_step += 1
+        st = self.sets[si]
+        row = self.b_hosts if in_place else self.b_dev[si]
+        # the slot of each layer's gather: a ring position, or the step's own buffer
+        if bs.one_layer:
+            slot_of = lambda i: i % self.ring  # noqa: E731
+        else:
+            own = (self.n_step - 1) % self.ring
+            slot_of = lambda i: own  # noqa: E731
+        # inputs: uploaded once the step that last used this set is done with them
+        self.h2d.wait_event(self.ev_free[si])
         with torch.cuda.stream(self.h2d):
-            b["tables"].copy_(self.h_tab, non_blocking=True)
+            st["tables"].copy_(self.h_tab, non_blocking=True)
             if not in_place:
-                b["hit"].copy_(self.t_hit, non_blocking=True)
-                b["miss"].copy_(self.t_miss, non_blocking=True)
-        self.ev_in.record(self.h2d)
-        s.wait_event(self.ev_in)
-        for bt in batches:
-            bt.plan(stream=s)
+                st["hit"].copy_(self.t_hit, non_blocking=True)
+                st["miss"].copy_(self.t_miss, non_blocking=True)
+        self.ev_in[si].record(self.h2d)
+        s.wait_event(self.ev_in[si])
+        for k in sorted({slot_of(i) for i in range(len(bs.groups))}):
+            row[k].plan(stream=s)
+            self.used.add(row[k])
+        batch = row[slot_of(0)]
         host = kvl.KVL_LAUNCH_HOST_SRC
         for i, (l0, n) in enumerate(bs.groups):
             batch.slice_layer(l0, bs.hit_views[l0], s, layer_count=n,
@@ -854,19 +877,19 @@ class EndToEnd:
         for i, (l0, n) in enumerate(bs.groups):
             batch.merge_scatter(l0, bs.pool, None, s, layer_count=n,
                                 flags=host if in_place else bs.flags("merge_scatter", i, l0))
-        self.ev_free.record(s)
+        self.ev_free[si].record(s)
         for i, (l0, n) in enumerate(bs.groups):
-            k = i % self.ring
+            k = slot_of(i)
             if bs.one_layer or i == 0:
                 s.wait_event(self.ev_slot[k])  # the slot's last objects have been read back
-            batches[k].gather(l0, bs.pool, s, layer_count=n, flags=bs.flags("gather", i, l0))
+            row[k].gather(l0, bs.pool, s, layer_count=n, flags=bs.flags("gather", i, l0))
             if bs.one_layer:
                 self._read_back(k, i % 2)
         if not bs.one_layer:
-            self._read_back(0, 0)
+            self._read_back(slot_of(0), 0)
         for i, (l0, n) in enumerate(bs.groups):
-            batches[i % self.ring].scatter_back(l0, bs.pool, s, layer_count=n,
-                                                flags=bs.flags("scatter_back", i, l0))
+            row[slot_of(i)].scatter_back(l0, bs.pool, s, layer_count=n,
+                                         flags=bs.flags("scatter_back", i, l0))
 
     def run(self, n, in_place):
         """n steps; returns seconds (CUDA events on the launch stream)."""
@@ -874,8 +897,7 @@ class EndToEnd:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(self.dev)
         e0.record(self.main)
-        self.ev_free.record(self.main)
-        for ev in self.ev_slot:
+        for ev in self.ev_free + self.ev_slot:
             ev.record(self.main)
         for _ in range(n):
             self._step(in_place)
@@ -883,7 +905,7 @@ class EndToEnd:
         self.main.wait_stream(self.d2h)
         e1.record(self.main)
         torch.cuda.synchronize(self.dev)
-        for bt in (self.b_hosts if in_place else self.b_dev):
+        for bt in self.used:
             check_status(bt, self.main, "in the end-to-end steps")
         return e0.elapsed_time(e1) / 1e3
 
@@ -938,9 +960,11 @@ class EndToEnd:
 
     def measure(self, steps, dist=None):
         """Both variants: link rates first, a warm-up step each, then `steps` timed
-        steps each.  Returns the e2e JSON object (staged as the headline)."""
+        steps each.  Returns the e2e JSON object (staged as the headline).  With several
+        ranks the bytes are every rank's and the time the slowest rank's."""
         spec = self.bs.spec
-        sb = step_bytes(spec)
+        ranks = 1 if dist is None else dist.get_world_size()
+        sb = sum_over_ranks(float(step_bytes(spec)), dist, self.dev)
         link = self.link_rates()
         out = {}
         for name, in_place in (("staged", False), ("in_place", True)):
@@ -951,16 +975,19 @@ class EndToEnd:
                 else self.h2d_bytes
             floor = link["floor_ms_per_step"] / 1e3 if not in_place else \
                 self.floor_s(link, link_in, self.d2h_bytes)
+            link_all = sum_over_ranks(float(link_in + self.d2h_bytes), dist, self.dev)
             out[name] = {"value": round(sb * steps / t / 1e9, 2), "unit": UNIT,
-                         "link_gbs": round((link_in + self.d2h_bytes) * steps / t / 1e9, 1),
+                         "link_gbs": round(link_all * steps / t / 1e9, 1),
                          "ms_per_step": round(t / steps * 1e3, 3), "steps": steps,
                          "link_in_bytes_per_step": int(link_in),
                          "link_out_bytes_per_step": int(self.d2h_bytes),
                          "floor_ms_per_step": round(floor * 1e3, 3),
                          "frac_of_floor": round(floor / (t / steps), 4)}
         st = out["staged"]
-        return {"value": st["value"], "unit": UNIT, "h2d_bytes_per_step": int(self.h2d_bytes),
-                "d2h_bytes_per_step": int(self.d2h_bytes), "steps": steps,
+        h2d = int(sum_over_ranks(float(self.h2d_bytes), dist, self.dev))
+        d2h = int(sum_over_ranks(float(self.d2h_bytes), dist, self.dev))
+        return {"value": st["value"], "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": steps, "ranks": ranks,
                 "ms_per_step": st["ms_per_step"], "link_gbs": st["link_gbs"],
                 "value_meaning": "HBM-algorithmic bytes of the step (as `value`) per second "
                                  "of the end-to-end step; link_gbs = bytes across the host "
@@ -972,6 +999,7 @@ class EndToEnd:
                         "gathered layer's objects -> pinned host as soon as it exists"
                         + (f" (a ring of {self.ring} device object layers, one plan each, "
                            "two host slots)" if self.bs.one_layer else " (all layers in one copy)")
+                        + f"; {self.n_sets} device input set(s) used in turn"
                         + "; in_place: the slice and merge-scatter read the host full block "
                           "and miss KV in place (KVL_LAUNCH_HOST_SRC), nothing staged"}
 
@@ -979,7 +1007,7 @@ class EndToEnd:
         for h in [self.h_hit, self.h_miss] + self.h_obj:
             h.__del__()
         self.t_hit = self.t_miss = self.t_obj = self.h_obj = None
-        self.d_obj = self.b_dev = self.b_hosts = self.b_host = None
+        self.d_obj = self.b_dev = self.b_hosts = self.b_host = self.sets = self.used = None
 
 
 def measure_host_leg(bs, e2e, dev):
@@ -1130,9 +1158,13 @@ def run_gpu(args):
     whole = bench_spec(args)
     log(f"workload {whole.name}: {step_bytes(whole) / 1e9:.1f} GB per step")
     part, spec = (None, whole) if world == 1 else rank_part(whole, world, rank)
-    if spec is None:
-        raise SystemExit(f"bench.py: rank {rank} of {world} has no part of {whole.name} "
-                         "(more ranks than requests and layers)")
+    if world > 1:
+        # every rank works out every rank's part (host arithmetic), so that all of them
+        # stop together, before any collective, if one would be left without work
+        idle = [r for r in range(world) if rank_part(whole, world, r)[1] is None]
+        if idle:
+            raise SystemExit(f"bench.py: ranks {idle} of {world} would have no part of "
+                             f"{whole.name} (more ranks than requests and layers)")
     clk = ClockSampler(local, Path(args.clocks_csv) if args.clocks_csv else None)
     ready = not args.no_plan_ready
     m = measure_step(spec, dev, steps=args.steps, warmup=args.warmup,
@@ -1153,7 +1185,7 @@ def run_gpu(args):
     ee = None
     if not args.no_e2e:
         try:
-            ee = EndToEnd(bs, dev)
+            ee = EndToEnd(bs, dev, two_sets=args.e2e_sets == 2)
         except MemoryError as exc:
             e2e = {"skipped": str(exc)}
             log(f"end to end skipped: {exc}")
@@ -1216,7 +1248,7 @@ def run_gpu(args):
             del mser["bs"]
             if name == PIPELINE_WORKLOAD and not args.no_e2e:
                 bs2.serial = False
-                ee = EndToEnd(bs2, dev)
+                ee = EndToEnd(bs2, dev, two_sets=args.e2e_sets == 2)
                 e = ee.measure(steps_for(side, 0.5, lo=5, hi=30))
                 entry["e2e"] = {k: e[k] for k in ("value", "link_gbs", "ms_per_step",
                                                   "h2d_bytes_per_step", "d2h_bytes_per_step",
@@ -1323,6 +1355,9 @@ def parse_args(argv=None):
     p.add_argument("--clocks-csv", default="",
                    help="also write the nvidia-smi clock samples of the timed region here")
     p.add_argument("--e2e-steps", type=int, default=4)
+    p.add_argument("--e2e-sets", type=int, default=2, choices=[1, 2],
+                   help="device input sets the staged end-to-end step alternates (2 where "
+                        "memory allows)")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-extras", action="store_true",

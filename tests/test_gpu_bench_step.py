@@ -238,7 +238,7 @@ def test_end_to_end_step_full_size(name, in_place):
         assert ob.gather_objects(0, host_pool) == 0
         return objs
 
-    assert ee.ring == (4 if one_layer else 1)
+    assert ee.ring == (4 if one_layer else ee.n_sets)
     for l in sampled:
         ob, objs, offs, host_pool = chk.problem(l)
         assert ob.merge_scatter(0, host_pool)[0] == 0
