@@ -980,9 +980,14 @@ class EndToEnd:
                          "link_gbs": round(link_all * steps / t / 1e9, 1),
                          "ms_per_step": round(t / steps * 1e3, 3), "steps": steps,
                          "link_in_bytes_per_step": int(link_in),
-                         "link_out_bytes_per_step": int(self.d2h_bytes),
-                         "floor_ms_per_step": round(floor * 1e3, 3),
-                         "frac_of_floor": round(floor / (t / steps), 4)}
+                         "link_out_bytes_per_step": int(self.d2h_bytes)}
+            if in_place:
+                # its inputs cross by SM loads, which can beat the copy engines' rates
+                out[name].update(copy_engine_floor_ms_per_step=round(floor * 1e3, 3),
+                                 frac_of_copy_engine_floor=round(floor / (t / steps), 4))
+            else:
+                out[name].update(floor_ms_per_step=round(floor * 1e3, 3),
+                                 frac_of_floor=round(floor / (t / steps), 4))
         st = out["staged"]
         h2d = int(sum_over_ranks(float(self.h2d_bytes), dist, self.dev))
         d2h = int(sum_over_ranks(float(self.d2h_bytes), dist, self.dev))
