@@ -88,8 +88,11 @@ class Layers:
         return out
 
 
-@pytest.mark.parametrize("name", FULL)
-def test_bench_step_full_size_every_layer(name):
+@pytest.mark.parametrize("name,serial", [(n, False) for n in FULL] + [("llama3_8b_agentic", True)],
+                         ids=FULL + ["llama3_8b_agentic-serial"])
+def test_bench_step_full_size_every_layer(name, serial):
+    """serial: every launch alone, each after the first prefetching before its wait
+    (KVL_LAUNCH_PLAN_READY), as the bench's serial step runs them."""
     import bench
     import layer_wise_paged_gb300 as kvl
     spec = workloads.get_spec(name)
@@ -97,7 +100,7 @@ def test_bench_step_full_size_every_layer(name):
     need = workloads.footprint_bytes(spec, objects_one_layer=one_layer) / 1e9
     if need + 12 + 4 * 3 > _free_gb():
         pytest.skip(f"{name} needs {need:.0f} GB of device memory, {_free_gb():.0f} GB free")
-    bs = bench.BenchStep(spec, "cuda")
+    bs = bench.BenchStep(spec, "cuda", serial=serial)
     assert bs.one_layer == one_layer
     L, ring = spec.L, bs.ring
     chk = Layers(spec, bs)
@@ -105,7 +108,13 @@ def test_bench_step_full_size_every_layer(name):
     phases = dict(bs.phases(bs.batch, s))
     flags = {op: [bs.flags(op, i, l0) for i, (l0, _) in enumerate(bs.groups)] for op in bench.OPS}
     # the launch flags are the bench's: overlapping after the first launch of a phase
-    assert any(flags["merge_scatter"])
+    # (serial: none overlapping, every one but the step's first prefetching)
+    if serial:
+        ov = kvl.KVL_LAUNCH_OVERLAP_PREVIOUS
+        assert not any(f & ov for fl in flags.values() for f in fl)
+        assert all(f & kvl.KVL_LAUNCH_PLAN_READY for f in flags["merge_scatter"])
+    else:
+        assert any(flags["merge_scatter"])
     bs.batch.plan(stream=s)
 
     # slice: a launch whose first layer reuses a ring buffer waits for the one before it,

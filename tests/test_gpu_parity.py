@@ -448,6 +448,24 @@ def test_merge_scatter_and_slice_read_a_host_full_block():
     assert gb.status() == (0, 0)
 
 
+def test_host_memory_launches_ignore_plan_ready():
+    """KVL_LAUNCH_PLAN_READY is accepted beside the host-memory flags and changes
+    nothing there: their launches read or write host memory with SM loads or stores
+    and keep the plain wait."""
+    import layer_wise_paged_gb300 as kvl
+    spec = workloads.custom_spec(**HOST_SPEC)
+    hb = host_buffers(spec)
+    gb, hit, miss, objects, pool = _host_batch(spec, hb, hit_host=True, miss_host=True)
+    ob = oracle_batch(spec, hb)
+    gb.plan()
+    for layer in range(spec.L):
+        f = kvl.KVL_LAUNCH_HOST_SRC | (kvl.KVL_LAUNCH_PLAN_READY if layer else 0)
+        gb.merge_scatter(layer, pool, flags=f)
+        assert ob.merge_scatter(layer, hb.pool)[0] == 0
+    assert_bytes_equal(pool, hb.pool, "pool")
+    assert gb.status() == (0, 0)
+
+
 def test_gather_writes_host_objects_and_scatter_back_reads_them():
     """Objects ready for transfer land in pinned host memory, and are restored from it."""
     import layer_wise_paged_gb300 as kvl
