@@ -766,19 +766,27 @@ class EndToEnd:
       over the link), so nothing is staged in HBM first.
 
     Launches are eager C-ABI calls from Python; copies run on their own streams.
-    Where device memory allows, the staged step alternates two device input sets: a
-    step's uploads go to the set the step before last used, once that step's
-    merge-scatter is done with it, so they run while the previous step still slices
-    and merges.  Object buffers are slots that a gather waits on only until the slot's
-    last read-back is done.  With all layers in one object buffer, each input set has
-    its own.  When all layers share one object layer (the largest workloads), the
-    gathers rotate over a ring of `ring` such layers, so read-backs trail the gathers;
-    scatter-back of layer l then reads slot l mod ring.  Each (input set, slot) pair
-    has its own batch and plan."""
+    Uploads overlap kernels in one of two ways:
 
-    def __init__(self, bs, dev, ring=4, two_sets=True):
+    * two device input sets, where device memory allows: a step's uploads go to the set
+      the step before last used, once that step's merge-scatter is done with it;
+    * otherwise the batch runs as two halves of its requests (split by bytes, over the
+      same buffers), one after the other, each half with its own launches: a half's
+      uploads wait only for that half's merge-scatter of the step before, so they run
+      while the other half's kernels run.
+
+    Object buffers are slots that a gather waits on only until its last read-back of
+    that slot is done.  With all layers in one object buffer each input set has its
+    own; when all layers share one object layer (the largest workloads), the gathers
+    rotate over a ring of `ring` such layers, so read-backs trail the gathers, and
+    scatter-back of layer l reads slot l mod ring.  Each half reads back only its own
+    requests' bytes of a slot.  Each (set, half, slot) has its own batch and plan; a
+    step builds all of its plans before its first copy launch."""
+
+    def __init__(self, bs, dev, ring=4, two_sets=True, halves=True):
         import torch
         from layer_wise_paged_gb300.batch import Batch, MappedHost
+        from layer_wise_paged_gb300.shard import request_weights, split_requests
         self.bs, self.dev = bs, dev
         b = bs.bufs
         n_obj = b["objects"].numel()
@@ -814,19 +822,46 @@ class EndToEnd:
         self.ring = max(1, min(int(ring), spec.L)) if bs.one_layer else self.n_sets
         self.d_obj = [b["objects"]] + [torch.full_like(b["objects"], workloads.SENTINEL)
                                        for _ in range(self.ring - 1)]
-        # batches: staged [set][slot], in place [slot] (their inputs are the host's)
-        self.b_dev = [[bs.batch if (si, k) == (0, 0) else
-                       Batch(g, lay.requests, st["hit"], st["miss"], o, st["tables"], b["src_tables"])
-                       for k, o in enumerate(self.d_obj)] for si, st in enumerate(self.sets)]
-        self.b_hosts = [Batch(g, lay.requests, self.h_hit, self.h_miss, o, b["tables"],
-                              b["src_tables"]) for o in self.d_obj]
-        self.b_host = self.b_hosts[0]
+        # halves of the batch (one input set only): request ranges split by bytes
+        n = spec.n_req
+        if self.n_sets == 1 and halves and n >= 2:
+            ranks = split_requests(request_weights(spec.t_hit, spec.t_miss, spec.B), 2)
+            cut = int(np.searchsorted(ranks, 1))
+            bounds = [(0, cut), (cut, n)] if 0 < cut < n else [(0, n)]
+        else:
+            bounds = [(0, n)]
+        blk_off = np.concatenate([[0], np.cumsum(spec.nblk())]).astype(np.int64)
+        hit_rows = np.concatenate([[0], np.cumsum(np.asarray(spec.t_hit, np.int64))])
+        reqs = lay.requests
+
+        def edge(i, field, total):
+            return getattr(reqs[i], field) if i < n else total
+
+        self.parts = []
+        for i0, i1 in bounds:
+            part = dict(reqs=reqs[i0:i1], hit=(edge(i0, "hit_off", lay.hit_bytes),
+                                               edge(i1, "hit_off", lay.hit_bytes)),
+                        miss=(edge(i0, "miss_off", lay.miss_bytes), edge(i1, "miss_off", lay.miss_bytes)),
+                        obj=(edge(i0, "obj_off", lay.obj_bytes), edge(i1, "obj_off", lay.obj_bytes)),
+                        tab=(int(blk_off[i0]), int(blk_off[i1])), hit_row0=int(hit_rows[i0]))
+            t0, t1 = part["tab"]
+            part["dev"] = [[Batch(g, part["reqs"], st["hit"], st["miss"], o, st["tables"][t0:t1],
+                                  b["src_tables"]) for o in self.d_obj] for st in self.sets]
+            part["host"] = [Batch(g, part["reqs"], self.h_hit, self.h_miss, o, b["tables"][t0:t1],
+                                  b["src_tables"]) for o in self.d_obj]
+            self.parts.append(part)
+        # the whole batch over the host inputs (the host legs use it)
+        self.b_host = Batch(g, reqs, self.h_hit, self.h_miss, self.d_obj[0], b["tables"],
+                            b["src_tables"])
         self.main = torch.cuda.current_stream(dev)
         self.h2d, self.d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         self.ev_g = torch.cuda.Event()
-        self.ev_in = [torch.cuda.Event() for _ in range(self.n_sets)]
-        self.ev_free = [torch.cuda.Event() for _ in range(self.n_sets)]  # set's inputs done with
-        self.ev_slot = [torch.cuda.Event() for _ in range(self.ring)]    # slot read back
+        keys = [(si, pi) for si in range(self.n_sets) for pi in range(len(self.parts))]
+        self.ev_tab = [torch.cuda.Event() for _ in range(self.n_sets)]  # a set's tables in place
+        self.ev_in = {k: torch.cuda.Event() for k in keys}              # a region's inputs in place
+        self.ev_free = {k: torch.cuda.Event() for k in keys}            # a region's inputs done with
+        self.ev_slot = {(pi, k): torch.cuda.Event() for pi in range(len(self.parts))
+                        for k in range(self.ring)}                      # a half's slot read back
         self.n_step = 0
         self.used = set()  # the batches steps have planned and used (their status is read)
         self.h2d_bytes = b["hit"].numel() + b["miss"].numel() + 4 * b["tables"].numel()
@@ -835,61 +870,82 @@ class EndToEnd:
         # bytes the in-place slice and merge-scatter read across the link per step
         self.in_place_bytes = (op_bytes(spec)["slice"] + op_bytes(spec)["merge_scatter"]) // 2 * spec.L
 
-    def _read_back(self, slot, host_slot):
+    def _read_back(self, pi, slot, host_slot):
         import torch
+        o0, o1 = self.parts[pi]["obj"]
         self.ev_g.record(self.main)
         self.d2h.wait_event(self.ev_g)
         with torch.cuda.stream(self.d2h):
-            self.t_obj[host_slot].copy_(self.d_obj[slot], non_blocking=True)
-        self.ev_slot[slot].record(self.d2h)
+            self.t_obj[host_slot][o0:o1].copy_(self.d_obj[slot][o0:o1], non_blocking=True)
+        self.ev_slot[(pi, slot)].record(self.d2h)
 
     def _step(self, in_place):
         import torch
         import layer_wise_paged_gb300 as kvl
         bs, s = self.bs, self.main
         si = 0 if in_place else self.n_step % self.n_sets
+        own = self.n_step % self.ring
         self.n_step += 1
         st = self.sets[si]
-        row = self.b_hosts if in_place else self.b_dev[si]
         # the slot of each layer's gather: a ring position, or the step's own buffer
-        if bs.one_layer:
-            slot_of = lambda i: i % self.ring  # noqa: E731
-        else:
-            own = (self.n_step - 1) % self.ring
-            slot_of = lambda i: own  # noqa: E731
-        # inputs: uploaded once the step that last used this set is done with them
-        self.h2d.wait_event(self.ev_free[si])
+        slot_of = (lambda i: i % self.ring) if bs.one_layer else (lambda i: own)
+        # uploads: the tables once the step that last used this set has planned (its
+        # first half's merge-scatter is later still), then each half's inputs once that
+        # half's merge-scatter of the step before is done with them
+        self.h2d.wait_event(self.ev_free[(si, 0)])
         with torch.cuda.stream(self.h2d):
             st["tables"].copy_(self.h_tab, non_blocking=True)
-            if not in_place:
-                st["hit"].copy_(self.t_hit, non_blocking=True)
-                st["miss"].copy_(self.t_miss, non_blocking=True)
-        self.ev_in[si].record(self.h2d)
-        s.wait_event(self.ev_in[si])
-        for k in sorted({slot_of(i) for i in range(len(bs.groups))}):
-            row[k].plan(stream=s)
-            self.used.add(row[k])
-        batch = row[slot_of(0)]
+        self.ev_tab[si].record(self.h2d)
+        for pi, part in enumerate(self.parts):
+            if in_place:
+                break
+            self.h2d.wait_event(self.ev_free[(si, pi)])
+            (h0, h1), (m0, m1) = part["hit"], part["miss"]
+            with torch.cuda.stream(self.h2d):
+                st["hit"][h0:h1].copy_(self.t_hit[h0:h1], non_blocking=True)
+                st["miss"][m0:m1].copy_(self.t_miss[m0:m1], non_blocking=True)
+            self.ev_in[(si, pi)].record(self.h2d)
+        # every plan of the step first, so that each copy launch after them follows a
+        # complete plan
+        s.wait_event(self.ev_tab[si])
+        slots = sorted({slot_of(i) for i in range(len(bs.groups))})
+        for part in self.parts:
+            rows = part["host"] if in_place else part["dev"][si]
+            for k in slots:
+                rows[k].plan(stream=s)
+                self.used.add(rows[k])
         host = kvl.KVL_LAUNCH_HOST_SRC
-        for i, (l0, n) in enumerate(bs.groups):
-            batch.slice_layer(l0, bs.hit_views[l0], s, layer_count=n,
-                              flags=host if in_place else bs.flags("slice", i, l0))
-        for i, (l0, n) in enumerate(bs.groups):
-            batch.merge_scatter(l0, bs.pool, None, s, layer_count=n,
-                                flags=host if in_place else bs.flags("merge_scatter", i, l0))
-        self.ev_free[si].record(s)
-        for i, (l0, n) in enumerate(bs.groups):
-            k = slot_of(i)
-            if bs.one_layer or i == 0:
-                s.wait_event(self.ev_slot[k])  # the slot's last objects have been read back
-            row[k].gather(l0, bs.pool, s, layer_count=n, flags=bs.flags("gather", i, l0))
-            if bs.one_layer:
-                self._read_back(k, i % 2)
-        if not bs.one_layer:
-            self._read_back(slot_of(0), 0)
-        for i, (l0, n) in enumerate(bs.groups):
-            row[slot_of(i)].scatter_back(l0, bs.pool, s, layer_count=n,
-                                         flags=bs.flags("scatter_back", i, l0))
+        layer_hit = bs.layer_hit
+        for pi, part in enumerate(self.parts):
+            rows = part["host"] if in_place else part["dev"][si]
+            if not in_place:
+                s.wait_event(self.ev_in[(si, pi)])
+            batch = rows[slot_of(0)]
+            off = part["hit_row0"] * bs.spec.R
+            for i, (l0, n) in enumerate(bs.groups):
+                hv = bs.hit_out[(l0 % bs.ring) * layer_hit + off:]
+                batch.slice_layer(l0, hv, s, layer_count=n,
+                                  flags=host if in_place else bs.flags("slice", i, l0))
+            for i, (l0, n) in enumerate(bs.groups):
+                batch.merge_scatter(l0, bs.pool, None, s, layer_count=n,
+                                    flags=host if in_place else bs.flags("merge_scatter", i, l0))
+            self.ev_free[(si, pi)].record(s)
+            for i, (l0, n) in enumerate(bs.groups):
+                k = slot_of(i)
+                if bs.one_layer or i == 0:
+                    s.wait_event(self.ev_slot[(pi, k)])  # this half's last read-back of the slot
+                rows[k].gather(l0, bs.pool, s, layer_count=n, flags=bs.flags("gather", i, l0))
+                if bs.one_layer:
+                    self._read_back(pi, k, i % 2)
+            if not bs.one_layer:
+                self._read_back(pi, slot_of(0), 0)
+            for i, (l0, n) in enumerate(bs.groups):
+                rows[slot_of(i)].scatter_back(l0, bs.pool, s, layer_count=n,
+                                              flags=bs.flags("scatter_back", i, l0))
+
+    def status_ok(self) -> bool:
+        """Every batch the steps used reports no error (reads back, synchronising)."""
+        return all(bt.status(self.main) == (0, 0) for bt in self.used)
 
     def run(self, n, in_place):
         """n steps; returns seconds (CUDA events on the launch stream)."""
@@ -897,7 +953,7 @@ class EndToEnd:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(self.dev)
         e0.record(self.main)
-        for ev in self.ev_free + self.ev_slot:
+        for ev in list(self.ev_free.values()) + list(self.ev_slot.values()):
             ev.record(self.main)
         for _ in range(n):
             self._step(in_place)
@@ -1004,7 +1060,10 @@ class EndToEnd:
                         "gathered layer's objects -> pinned host as soon as it exists"
                         + (f" (a ring of {self.ring} device object layers, one plan each, "
                            "two host slots)" if self.bs.one_layer else " (all layers in one copy)")
-                        + f"; {self.n_sets} device input set(s) used in turn"
+                        + (f"; {self.n_sets} device input sets used in turn" if self.n_sets > 1
+                           else f"; the batch in {len(self.parts)} halves of its requests, "
+                                "each half's uploads overlapping the other's kernels"
+                           if len(self.parts) > 1 else "")
                         + "; in_place: the slice and merge-scatter read the host full block "
                           "and miss KV in place (KVL_LAUNCH_HOST_SRC), nothing staged"}
 
@@ -1012,7 +1071,7 @@ class EndToEnd:
         for h in [self.h_hit, self.h_miss] + self.h_obj:
             h.__del__()
         self.t_hit = self.t_miss = self.t_obj = self.h_obj = None
-        self.d_obj = self.b_dev = self.b_hosts = self.b_host = self.sets = self.used = None
+        self.d_obj = self.parts = self.b_host = self.sets = self.used = None
 
 
 def measure_host_leg(bs, e2e, dev):

@@ -199,8 +199,10 @@ def test_end_to_end_step_full_size(name, in_place):
     """One end-to-end step as bench.py times it: the inputs uploaded from pinned host
     memory (or read there in place by the slice and merge-scatter), the objects read
     back to pinned host memory layer by layer (through a ring of device object slots
-    when all layers share one object layer).  Sampled layers of hit_layer, the pool and
-    the objects read back are compared with the oracle."""
+    when all layers share one object layer; the 256-request batch in two halves of its
+    requests, one input set; the Llama turn alternating two input sets).  Sampled
+    layers of hit_layer, the pool and the objects read back are compared with the
+    oracle."""
     import bench
     spec = workloads.get_spec(name)
     one_layer = workloads.footprint_bytes(spec) > 160e9
@@ -219,7 +221,7 @@ def test_end_to_end_step_full_size(name, in_place):
         bs.bufs["hit"].zero_()
         bs.bufs["miss"].zero_()
     ee.run(1, in_place)
-    assert (ee.b_host if in_place else bs.batch).status() == (0, 0)
+    assert ee.status_ok()
     if not in_place:  # the uploads restored the inputs the oracle reads
         assert np.array_equal(bs.bufs["hit"][:1 << 20].cpu().numpy(), ee.h_hit.np[:1 << 20])
     sampled = sorted({L - bs.ring, L - 2, L - 1})
@@ -248,6 +250,7 @@ def test_end_to_end_step_full_size(name, in_place):
         return objs
 
     assert ee.ring == (4 if one_layer else ee.n_sets)
+    assert len(ee.parts) == (2 if ee.n_sets == 1 else 1)
     for l in sampled:
         ob, objs, offs, host_pool = chk.problem(l)
         assert ob.merge_scatter(0, host_pool)[0] == 0
