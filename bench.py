@@ -60,6 +60,7 @@ PIPELINE_WORKLOAD = "llama3_8b_agentic"  # host legs and the overlap with comput
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, about 8 TB/s (context for "% of peak")
 HIT_RING = 8
+E2E_PARTS = 8  # parts of the batch in the staged end-to-end step (one input set)
 KERNEL_REPS = 11  # replays whose per-phase events give the per-kernel median
 OPS = ("slice", "merge_scatter", "gather", "scatter_back")
 KERNEL_NAMES = {"slice": "kvl_slice_kernel", "merge_scatter": "kvl_merge_scatter_kernel",
@@ -753,6 +754,19 @@ def step_summary(spec, m, peak):
             "frac_of_nominal": round(m["per_op"][dom]["gbs"] / NOMINAL_HBM_GBS, 4)}
 
 
+def request_parts(spec, k):
+    """The batch as at most k contiguous request ranges [a, z), none empty, balanced by
+    each request's step bytes with the batch split's midpoint rule."""
+    from layer_wise_paged_gb300.shard import request_weights, split_requests
+    n = spec.n_req
+    k = max(1, min(int(k), n))
+    if k == 1:
+        return [(0, n)]
+    ranks = split_requests(request_weights(spec.t_hit, spec.t_miss, spec.B), k)
+    cuts = [0] + [int(np.searchsorted(ranks, r)) for r in range(1, k)] + [n]
+    return [(a, z) for a, z in zip(cuts[:-1], cuts[1:]) if z > a]
+
+
 class EndToEnd:
     """The bench step through the C ABI with its inputs in pinned host memory (Grace
     memory, over NVLink-C2C) and its objects read back to pinned host memory, every
@@ -770,23 +784,22 @@ class EndToEnd:
 
     * two device input sets, where device memory allows: a step's uploads go to the set
       the step before last used, once that step's merge-scatter is done with it;
-    * otherwise the batch runs as two halves of its requests (split by bytes, over the
-      same buffers), one after the other, each half with its own launches: a half's
-      uploads wait only for that half's merge-scatter of the step before, so they run
-      while the other half's kernels run.
+    * otherwise the batch runs as `parts` parts of its requests (contiguous runs split
+      by bytes, over the same buffers), one after the other, each part with its own
+      launches: a part's uploads wait only for that part's merge-scatter of the step
+      before, so they run while the other parts' kernels run.
 
     Object buffers are slots that a gather waits on only until its last read-back of
     that slot is done.  With all layers in one object buffer each input set has its
     own; when all layers share one object layer (the largest workloads), the gathers
     rotate over a ring of `ring` such layers, so read-backs trail the gathers, and
-    scatter-back of layer l reads slot l mod ring.  Each half reads back only its own
-    requests' bytes of a slot.  Each (set, half, slot) has its own batch and plan; a
+    scatter-back of layer l reads slot l mod ring.  Each part reads back only its own
+    requests' bytes of a slot.  Each (set, part, slot) has its own batch and plan; a
     step builds all of its plans before its first copy launch."""
 
-    def __init__(self, bs, dev, ring=4, two_sets=True, halves=True):
+    def __init__(self, bs, dev, ring=4, two_sets=True, parts=None):
         import torch
         from layer_wise_paged_gb300.batch import Batch, MappedHost
-        from layer_wise_paged_gb300.shard import request_weights, split_requests
         self.bs, self.dev = bs, dev
         b = bs.bufs
         n_obj = b["objects"].numel()
@@ -822,14 +835,10 @@ class EndToEnd:
         self.ring = max(1, min(int(ring), spec.L)) if bs.one_layer else self.n_sets
         self.d_obj = [b["objects"]] + [torch.full_like(b["objects"], workloads.SENTINEL)
                                        for _ in range(self.ring - 1)]
-        # halves of the batch (one input set only): request ranges split by bytes
+        # parts of the batch (one input set only): request ranges split by bytes
         n = spec.n_req
-        if self.n_sets == 1 and halves and n >= 2:
-            ranks = split_requests(request_weights(spec.t_hit, spec.t_miss, spec.B), 2)
-            cut = int(np.searchsorted(ranks, 1))
-            bounds = [(0, cut), (cut, n)] if 0 < cut < n else [(0, n)]
-        else:
-            bounds = [(0, n)]
+        bounds = request_parts(spec, E2E_PARTS if parts is None else parts) \
+            if self.n_sets == 1 else [(0, n)]
         blk_off = np.concatenate([[0], np.cumsum(spec.nblk())]).astype(np.int64)
         hit_rows = np.concatenate([[0], np.cumsum(np.asarray(spec.t_hit, np.int64))])
         reqs = lay.requests
@@ -861,7 +870,7 @@ class EndToEnd:
         self.ev_in = {k: torch.cuda.Event() for k in keys}              # a region's inputs in place
         self.ev_free = {k: torch.cuda.Event() for k in keys}            # a region's inputs done with
         self.ev_slot = {(pi, k): torch.cuda.Event() for pi in range(len(self.parts))
-                        for k in range(self.ring)}                      # a half's slot read back
+                        for k in range(self.ring)}                      # a part's slot read back
         self.n_step = 0
         self.used = set()  # the batches steps have planned and used (their status is read)
         self.h2d_bytes = b["hit"].numel() + b["miss"].numel() + 4 * b["tables"].numel()
@@ -890,8 +899,8 @@ class EndToEnd:
         # the slot of each layer's gather: a ring position, or the step's own buffer
         slot_of = (lambda i: i % self.ring) if bs.one_layer else (lambda i: own)
         # uploads: the tables once the step that last used this set has planned (its
-        # first half's merge-scatter is later still), then each half's inputs once that
-        # half's merge-scatter of the step before is done with them
+        # first part's merge-scatter is later still), then each part's inputs once that
+        # part's merge-scatter of the step before is done with them
         self.h2d.wait_event(self.ev_free[(si, 0)])
         with torch.cuda.stream(self.h2d):
             st["tables"].copy_(self.h_tab, non_blocking=True)
@@ -933,7 +942,7 @@ class EndToEnd:
             for i, (l0, n) in enumerate(bs.groups):
                 k = slot_of(i)
                 if bs.one_layer or i == 0:
-                    s.wait_event(self.ev_slot[(pi, k)])  # this half's last read-back of the slot
+                    s.wait_event(self.ev_slot[(pi, k)])  # this part's last read-back of the slot
                 rows[k].gather(l0, bs.pool, s, layer_count=n, flags=bs.flags("gather", i, l0))
                 if bs.one_layer:
                     self._read_back(pi, k, i % 2)
@@ -1021,12 +1030,21 @@ class EndToEnd:
         spec = self.bs.spec
         ranks = 1 if dist is None else dist.get_world_size()
         sb = sum_over_ranks(float(step_bytes(spec)), dist, self.dev)
-        link = self.link_rates()
-        out = {}
+        before = self.link_rates()
+        runs = {}
         for name, in_place in (("staged", False), ("in_place", True)):
             self.run(1, in_place)
             barrier(dist, self.dev)
-            t = max_over_ranks(self.run(steps, in_place), dist, self.dev)
+            runs[name] = max_over_ranks(self.run(steps, in_place), dist, self.dev)
+        after = self.link_rates()
+        # the link's rate drifts on some boxes: the floor takes the faster of the two
+        # measurements on each side of the timed steps, so a slow spell cannot lower it
+        link = {k: max(before[k], after[k]) for k in ("h2d_gbs", "d2h_gbs", "both_gbs")}
+        link["floor_ms_per_step"] = min(before["floor_ms_per_step"], after["floor_ms_per_step"])
+        link["before"], link["after"] = before, after
+        out = {}
+        for name, in_place in (("staged", False), ("in_place", True)):
+            t = runs[name]
             link_in = (self.in_place_bytes + 4 * self.bs.bufs["tables"].numel()) if in_place \
                 else self.h2d_bytes
             floor = link["floor_ms_per_step"] / 1e3 if not in_place else \
@@ -1061,8 +1079,8 @@ class EndToEnd:
                         + (f" (a ring of {self.ring} device object layers, one plan each, "
                            "two host slots)" if self.bs.one_layer else " (all layers in one copy)")
                         + (f"; {self.n_sets} device input sets used in turn" if self.n_sets > 1
-                           else f"; the batch in {len(self.parts)} halves of its requests, "
-                                "each half's uploads overlapping the other's kernels"
+                           else f"; the batch in {len(self.parts)} parts of its requests, "
+                                "each part's uploads overlapping the other parts' kernels"
                            if len(self.parts) > 1 else "")
                         + "; in_place: the slice and merge-scatter read the host full block "
                           "and miss KV in place (KVL_LAUNCH_HOST_SRC), nothing staged"}
@@ -1249,7 +1267,7 @@ def run_gpu(args):
     ee = None
     if not args.no_e2e:
         try:
-            ee = EndToEnd(bs, dev, two_sets=args.e2e_sets == 2)
+            ee = EndToEnd(bs, dev, two_sets=args.e2e_sets == 2, parts=args.e2e_parts)
         except MemoryError as exc:
             e2e = {"skipped": str(exc)}
             log(f"end to end skipped: {exc}")
@@ -1312,7 +1330,7 @@ def run_gpu(args):
             del mser["bs"]
             if name == PIPELINE_WORKLOAD and not args.no_e2e:
                 bs2.serial = False
-                ee = EndToEnd(bs2, dev, two_sets=args.e2e_sets == 2)
+                ee = EndToEnd(bs2, dev, two_sets=args.e2e_sets == 2, parts=args.e2e_parts)
                 e = ee.measure(steps_for(side, 0.5, lo=5, hi=30))
                 entry["e2e"] = {k: e[k] for k in ("value", "link_gbs", "ms_per_step",
                                                   "h2d_bytes_per_step", "d2h_bytes_per_step",
@@ -1422,6 +1440,9 @@ def parse_args(argv=None):
     p.add_argument("--e2e-sets", type=int, default=2, choices=[1, 2],
                    help="device input sets the staged end-to-end step alternates (2 where "
                         "memory allows)")
+    p.add_argument("--e2e-parts", type=int, default=E2E_PARTS,
+                   help="with one device input set, the staged end-to-end step runs the batch "
+                        "as this many byte-balanced parts of its requests")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-extras", action="store_true",

@@ -88,6 +88,29 @@ def test_plan_ready_goes_on_every_waiting_launch_but_the_first_after_the_plan():
     assert _flags("merge_scatter", 3, serial=True) == [0] * 3
 
 
+@pytest.mark.parametrize("k", [1, 2, 8, 300])
+@pytest.mark.parametrize("name", ["many_small", "latent_batch", "llama3_8b_agentic"])
+def test_end_to_end_parts_cover_the_requests_in_order(name, k):
+    from layer_wise_paged_gb300.shard import request_weights
+    spec = workloads.get_spec(name)
+    parts = bench.request_parts(spec, k)
+    n = spec.n_req
+    # the midpoint rule can leave a rank empty only when parts are about as many as
+    # requests; empty parts are dropped
+    assert 1 <= len(parts) <= min(k, n)
+    if k <= 8:
+        assert len(parts) == min(k, n)
+    # contiguous, non-empty, in order, every request once
+    assert parts[0][0] == 0 and parts[-1][1] == n
+    assert all(a < z for a, z in parts)
+    assert all(parts[i][1] == parts[i + 1][0] for i in range(len(parts) - 1))
+    # the midpoint rule's bound: each part within the largest request of an equal share
+    w = request_weights(spec.t_hit, spec.t_miss, spec.B)
+    share = w.sum() / min(k, n)
+    for a, z in parts:
+        assert abs(int(w[a:z].sum()) - share) <= int(w.max())
+
+
 def test_traffic_record_is_read_only_for_the_current_kernel_source():
     h = bench.kernel_source_hash()
     rec = [line.split() for line in (bench.ROOT / "profiles" / "dram_traffic.txt").read_text()

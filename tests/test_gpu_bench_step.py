@@ -199,8 +199,8 @@ def test_end_to_end_step_full_size(name, in_place):
     """One end-to-end step as bench.py times it: the inputs uploaded from pinned host
     memory (or read there in place by the slice and merge-scatter), the objects read
     back to pinned host memory layer by layer (through a ring of device object slots
-    when all layers share one object layer; the 256-request batch in two halves of its
-    requests, one input set; the Llama turn alternating two input sets).  Sampled
+    when all layers share one object layer; the 256-request batch in byte-balanced parts
+    of its requests, one input set; the Llama turn alternating two input sets).  Sampled
     layers of hit_layer, the pool and the objects read back are compared with the
     oracle."""
     import bench
@@ -250,7 +250,7 @@ def test_end_to_end_step_full_size(name, in_place):
         return objs
 
     assert ee.ring == (4 if one_layer else ee.n_sets)
-    assert len(ee.parts) == (2 if ee.n_sets == 1 else 1)
+    assert len(ee.parts) == (bench.E2E_PARTS if ee.n_sets == 1 else 1)
     for l in sampled:
         ob, objs, offs, host_pool = chk.problem(l)
         assert ob.merge_scatter(0, host_pool)[0] == 0
