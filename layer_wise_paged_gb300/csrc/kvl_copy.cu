@@ -11,8 +11,10 @@
 // SM of a persistent grid:
 //   * scheduling: CTA b takes items b and b + G, then claims further items one at a
 //     time from a per-(layer, op) counter in the plan (atomicAdd, issued one item
-//     ahead), so faster SMs take more items and all finish together; the last CTA to
-//     finish resets the counter for the next launch;
+//     ahead), so faster SMs take more items and all finish together; every CTA stops
+//     after its first claim past the end, so a launch's claims are counted in advance,
+//     and the CTA that draws the last of them rewinds the counter for the next launch
+//     (no CTA waits on an atomic on its way out);
 //   * metadata: the plan resolved every item into a 128-byte record (bases and
 //     strides at layer 0, pool block id, hit / valid slot counts); the warp loads the
 //     next item's record (one word per lane) while the current item's copies run,
@@ -699,15 +701,33 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
     const int64_t nxt_static = blockIdx.x + G;
     // unit cur < n_items is item cur of the first layer: the record read above
     uint32_t rec_cur = cur < n_items ? rec_first : cur < n_units ? load_rec(item_of(cur)) : 0u;
+    // Every CTA claims until its first claim past the last unit and then stops, so a
+    // launch draws exactly max(n_units - 2G, 0) + G claims, numbered from 0.  The CTA
+    // that reads the last of them rewinds the counter for the next launch on it: no
+    // claim of this launch can follow.  (A launch in which some CTA stops early, on a
+    // timeout or on a plan status that turned to an error, may leave the counter
+    // unrewound; its plan then carries that error, which makes every later copy call
+    // on it a no-op until the plan is rebuilt, and a rebuild clears the counters.)
+    const uint32_t last_claim = uint32_t((n_units > 2 * G ? n_units - 2 * G : 0) + G - 1);
     uint32_t claim = 0;
+    bool claim_unread = true;
     if (lane == 0) claim = atomicAdd(&ctr->next, 1u);
+    auto read_claim = [&]() -> uint32_t {
+        const uint32_t c = __shfl_sync(0xffffffffu, claim, 0);
+        if (claim_unread && c == last_claim && lane == 0) atomicExch(&ctr->next, 0u);
+        claim_unread = false;
+        return c;
+    };
     for (bool first = true;; first = false) {
         int64_t nxt;
         if (first) {
             nxt = nxt_static;
         } else {
-            nxt = 2 * G + int64_t(__shfl_sync(0xffffffffu, claim, 0));
-            if (nxt < n_units && lane == 0) claim = atomicAdd(&ctr->next, 1u);
+            nxt = 2 * G + int64_t(read_claim());
+            if (nxt < n_units) {
+                if (lane == 0) claim = atomicAdd(&ctr->next, 1u);
+                claim_unread = true;
+            }
         }
         uint32_t rec_nxt = 0;
         if (nxt < n_units) rec_nxt = load_rec(item_of(nxt));
@@ -803,6 +823,8 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
         rec_cur = rec_nxt;
     }
     while (retired < issued && !timed_out) retire();
+    // a CTA that had no unit to take after its first claim still reads it
+    if (claim_unread) read_claim();
 
     if (timed_out) {
         if (lane == 0) record_error(h, KVL_ETIMEOUT, (unsigned long long)blockIdx.x);
@@ -812,14 +834,8 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
     }
     bulk_wait_all();
     __syncwarp();
-    if (lane == 0) {
+    if (lane == 0)
         for (int s = 0; s < kStages; ++s) mbar_inval(bar0 + 8 * s);
-        // the last CTA of this launch resets the counter for the next launch
-        if (atomicAdd(&ctr->done, 1u) == uint32_t(G) - 1u) {
-            atomicExch(&ctr->next, 0u);
-            atomicExch(&ctr->done, 0u);
-        }
-    }
     if (overlap) grid_dependency_wait();
 }
 

@@ -71,10 +71,10 @@ struct ItemRec {
 };
 static_assert(sizeof(ItemRec) == 128, "item record layout");
 
-// Work-claim counters of one (layer, op): the next item to claim and the CTAs done.
+// Work-claim counter of one (layer, op): the next claim's number (0 between launches).
 struct ClaimCounter {
     uint32_t next;
-    uint32_t done;
+    uint32_t reserved;  // kept 0: holds the counter section at 8 bytes per (layer, op)
 };
 
 constexpr size_t kRecordsOffset = 256;  // the item records start right after the header

@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kScanThreads) plan_scan_kernel(PlanArgs a)
     }
     for (int64_t c = tid; c < int64_t(a.L) * kOps; c += kScanThreads) {
         a.v.counters[c].next = 0u;
-        a.v.counters[c].done = 0u;
+        a.v.counters[c].reserved = 0u;
     }
     if (a.check_injective) {
         const int64_t words = (a.N + 31) / 32;

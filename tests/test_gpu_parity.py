@@ -357,6 +357,57 @@ def test_an_sm_budget_changes_nothing_but_speed(max_ctas):
     assert gb.status() == (0, 0)
 
 
+def _claim_counters(gb):
+    """The plan's per-(layer, op) claim counters, [L][4] x (next, reserved)."""
+    off = gb.layout[7]
+    return gb.d_plan[off:off + gb.L * 4 * 8].cpu().numpy().view(np.uint32).reshape(gb.L, 4, 2)
+
+
+# 26 work items per layer: the CTA caps below give fewer items than CTAs (whole GPU,
+# 40), between one and two per CTA (20), exactly two (13) and more (5, 1), so the
+# launch's count of claims, max(units - 2G, 0) + G, takes each of its forms.
+@pytest.mark.parametrize("max_ctas", [None, 40, 20, 13, 5, 1])
+@pytest.mark.parametrize("layer_count", [1, 2])
+def test_repeated_launches_on_one_plan_rewind_their_claim_counters(max_ctas, layer_count):
+    spec = workloads.custom_spec(L=3, P=2, B=16, Rp=512, t_hit=[300, 66], t_miss=[20, 30],
+                                 source="contiguous", seed=71)
+    hb = host_buffers(spec)
+    gb, d = device_batch(spec, hb)
+    ob = oracle_batch(spec, hb)
+    gb.plan()
+    assert gb.n_items == 26
+    R, l0 = spec.R, 1
+    n_hit = ob.total_hit() * R
+    want_hit = np.concatenate([ob.slice_layer(l)[1] for l in range(l0, l0 + layer_count)])
+    for l in range(l0, l0 + layer_count):
+        assert ob.merge_scatter(l, hb.pool)[0] == 0
+        assert ob.gather_objects(l, hb.pool) == 0
+    pool_want, obj_want = hb.pool.copy(), hb.objects.copy()
+    pool0 = d.pool.clone()
+    for rep in range(3):
+        # each launch starts from a fresh destination, so every byte is this launch's
+        hit_out = sentinel_dev(layer_count * n_hit)
+        gb.slice_layer(l0, hit_out, layer_count=layer_count, max_ctas=max_ctas)
+        assert_bytes_equal(hit_out[:want_hit.size], want_hit, f"hit_out, launch {rep}")
+        assert not _claim_counters(gb).any(), f"counters after slice launch {rep}"
+        d.pool.copy_(pool0)
+        gb.merge_scatter(l0, d.pool, layer_count=layer_count, max_ctas=max_ctas)
+        d.objects.fill_(SENT)
+        gb.gather(l0, d.pool, layer_count=layer_count, max_ctas=max_ctas)
+        assert_bytes_equal(d.pool, pool_want, f"pool, launch {rep}")
+        assert_bytes_equal(d.objects, obj_want, f"objects, launch {rep}")
+        assert not _claim_counters(gb).any(), f"counters after merge and gather {rep}"
+        d.pool.fill_(SENT)
+        gb.scatter_back(l0, d.pool, layer_count=layer_count, max_ctas=max_ctas)
+        back = hb.pool.copy()
+        back[:] = SENT
+        for l in range(l0, l0 + layer_count):
+            assert ob.scatter_back(l, back) == 0
+        assert_bytes_equal(d.pool, back, f"pool after scatter-back, launch {rep}")
+        assert not _claim_counters(gb).any(), f"counters after scatter-back {rep}"
+    assert gb.status() == (0, 0)
+
+
 @pytest.mark.parametrize("budgets", [(None,), (5, None, 2, 11)])
 def test_overlapped_layer_launches_equal_the_oracle(budgets):
     """Each op's launches for successive layers carry KVL_LAUNCH_OVERLAP_PREVIOUS (all
