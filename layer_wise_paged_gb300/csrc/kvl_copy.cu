@@ -41,8 +41,9 @@
 // (KVL_LAUNCH_OVERLAP_PREVIOUS), it lets its successor launch at once and waits just
 // before it exits, so it still completes after its predecessor.  With a plan the
 // caller declared complete (KVL_LAUNCH_PLAN_READY), a waiting kernel checks the plan,
-// reads its first records, acquires its first tensor maps and prefetches its first
-// source rows into L2 (cp.async.bulk.prefetch) before the wait.
+// reads its first records, acquires its first tensor maps, prefetches its first
+// source rows into L2 (cp.async.bulk.prefetch) and decodes its first unit's addresses
+// before the wait.
 #include <cstdint>
 
 #include "kvl_internal.cuh"
@@ -459,6 +460,18 @@ __device__ __forceinline__ bool item_meta(const CopyArgs &a, PlanHeader *h, cons
     return true;
 }
 
+// grid_dependency_wait with the fields of `m` the first copies use as operands, so
+// that they are computed before the wait rather than after it.
+__device__ __forceinline__ void grid_dependency_wait_after(const ItemMeta &m)
+{
+#if KVL_PDL
+    asm volatile("griddepcontrol.wait;" ::"l"(m.src_a), "l"(m.src_b), "l"(m.dst), "l"(m.map_a),
+                 "l"(m.a_stride), "l"(m.dst_pstride), "r"(m.n_valid), "r"(m.n_a), "r"(m.tok_a),
+                 "r"(m.blk_a)
+                 : "memory");
+#endif
+}
+
 // Prefetch into L2 the source bytes unit (rec, layer l) will read first, at most
 // `budget` of them; returns the bytes asked for.  Token rows of the slice and
 // merge-scatter (a row's P planes are adjacent in both sources: R bytes), whole
@@ -572,6 +585,10 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
     // lane 0's four most recently acquired maps, newest first
     const uint8_t *acq0 = nullptr, *acq1 = nullptr, *acq2 = nullptr, *acq3 = nullptr;
     bool header_read = false;
+    // the first unit's addresses, worked out before the wait by a launch with a
+    // complete plan (decoding a record takes a few hundred cycles of one warp)
+    ItemMeta m_first = {};
+    bool m_first_ready = false, m_first_ok = false;
     if (early) {
         // The plan was complete before the previous kernel began: a status of OK now
         // means every item record was written, and the records never change after.
@@ -612,8 +629,13 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
                     }
                 }
             }
+            if (int64_t(blockIdx.x) < n_items) {  // unit blockIdx.x: item blockIdx.x, first layer
+                m_first_ok = item_meta<OP>(a, h, map_chunk > 0 ? v.maps : nullptr, rec_first,
+                                           a.layer, n_hit_all, n_tok_all, m_first);
+                m_first_ready = true;
+            }
         }
-        grid_dependency_wait();
+        grid_dependency_wait_after(m_first);
         allow_dependents_launch();
     }
     usable = usable && h->status == KVL_OK;
@@ -708,10 +730,17 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
     // timeout or on a plan status that turned to an error, may leave the counter
     // unrewound; its plan then carries that error, which makes every later copy call
     // on it a no-op until the plan is rebuilt, and a rebuild clears the counters.)
+    // A CTA draws its first claim once its first load is on its way (or when it has no
+    // load to issue): every CTA of a launch draws it at about the same moment, so the
+    // atomics queue at the counter, and nothing before the first load waits for one.
     const uint32_t last_claim = uint32_t((n_units > 2 * G ? n_units - 2 * G : 0) + G - 1);
     uint32_t claim = 0;
-    bool claim_unread = true;
-    if (lane == 0) claim = atomicAdd(&ctr->next, 1u);
+    bool claim_unread = false, first_claim_due = true;
+    auto draw_claim = [&]() {
+        if (lane == 0) claim = atomicAdd(&ctr->next, 1u);
+        claim_unread = true;
+        first_claim_due = false;
+    };
     auto read_claim = [&]() -> uint32_t {
         const uint32_t c = __shfl_sync(0xffffffffu, claim, 0);
         if (claim_unread && c == last_claim && lane == 0) atomicExch(&ctr->next, 0u);
@@ -723,11 +752,9 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
         if (first) {
             nxt = nxt_static;
         } else {
+            if (first_claim_due) draw_claim();  // the first unit issued no load
             nxt = 2 * G + int64_t(read_claim());
-            if (nxt < n_units) {
-                if (lane == 0) claim = atomicAdd(&ctr->next, 1u);
-                claim_unread = true;
-            }
+            if (nxt < n_units) draw_claim();
         }
         uint32_t rec_nxt = 0;
         if (nxt < n_units) rec_nxt = load_rec(item_of(nxt));
@@ -735,7 +762,14 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
 
         ItemMeta m;
         const int64_t l_cur = layer_of(cur);
-        if (item_meta<OP>(a, h, maps, rec_cur, l_cur, n_hit_all, n_tok_all, m)) {
+        bool meta_ok;
+        if (first && m_first_ready) {
+            m = m_first;
+            meta_ok = m_first_ok;
+        } else {
+            meta_ok = item_meta<OP>(a, h, maps, rec_cur, l_cur, n_hit_all, n_tok_all, m);
+        }
+        if (meta_ok) {
           for (int p = 0; p < planes && !timed_out; ++p) {
             for (int s0 = 0; s0 < m.n_valid && !timed_out; s0 += max_rows) {
                 const int ns = m.n_valid - s0 < max_rows ? m.n_valid - s0 : max_rows;
@@ -816,6 +850,7 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
                     }
                 }
                 ++issued;
+                if (first_claim_due) draw_claim();
             }
           }
         }
@@ -823,7 +858,8 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
         rec_cur = rec_nxt;
     }
     while (retired < issued && !timed_out) retire();
-    // a CTA that had no unit to take after its first claim still reads it
+    // a CTA with no unit of its own still draws its claim, and every CTA reads its last
+    if (first_claim_due) draw_claim();
     if (claim_unread) read_claim();
 
     if (timed_out) {
