@@ -150,9 +150,9 @@ typedef struct kvl_launch {
  * kernel that may still run writes it, other than the copy calls' own claim counters
  * and status word.  True of every copy call of a layer-wise pipeline except the first
  * one after kvl_batch_plan.  A call that must wait for the kernel before it (no
- * KVL_LAUNCH_OVERLAP_PREVIOUS) then checks the plan, reads its first work items and
- * prefetches their source rows into L2 (cp.async.bulk.prefetch) while that kernel
- * drains, and waits only before its first copy; L2 is the device's point of
+ * KVL_LAUNCH_OVERLAP_PREVIOUS) then checks the plan, reads and decodes its first work
+ * items and prefetches their source rows into L2 (cp.async.bulk.prefetch) while that
+ * kernel drains, and waits only before its first copy; L2 is the device's point of
  * coherence, so rows the previous kernel writes are still read as it leaves them.
  * Results are the same with or without the flag; with a plan that is not complete,
  * undefined.  Ignored with KVL_LAUNCH_OVERLAP_PREVIOUS and by the host-memory
