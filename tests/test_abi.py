@@ -145,6 +145,26 @@ def test_copy_calls_refuse_a_plan_smaller_than_the_geometry_needs(lib):
     assert kvl.kvl_merge_scatter_paged(g, fake, least - 1, fake, fake, 0, 1, fake + 4) == kvl.KVL_EINVAL
 
 
+def test_unit_numbering_limits_are_refused_on_the_host(lib):
+    """Block ids are int32 and a launch numbers its (layer, item) units in 32 bits: a
+    geometry with more than INT32_MAX pool blocks is refused by every call, and a copy
+    call whose pool_blocks x layer_count reaches 2^31 returns KVL_EINVAL before any
+    launch; one layer fewer passes that check (a misaligned pool answers instead)."""
+    fake = 1 << 20  # never dereferenced: each call below is refused on the host
+    too_many = kvl.geom(4, 2, 16, 256, (1 << 31))
+    assert kvl.kvl_plan_bytes(too_many, 1) == 0
+    assert kvl.kvl_merge_scatter_paged(too_many, fake, 1 << 62, fake, fake, 0, 1, fake) == kvl.KVL_EINVAL
+    g = kvl.geom(4, 2, 16, 256, 1 << 30)
+    least = kvl.kvl_plan_layout(g, 0)[8]
+    for call in (lambda lc, pool: kvl.kvl_merge_scatter_paged(g, fake, least, fake, fake, 0, lc, pool),
+                 lambda lc, pool: kvl.kvl_gather_layer_objects(g, fake, least, fake, fake, 0, lc, pool,
+                                                               kvl.KVL_GATHER)):
+        assert call(2, fake) == kvl.KVL_EINVAL      # 2^30 blocks x 2 layers = 2^31 units
+        assert call(1, fake + 4) == kvl.KVL_EALIGN  # 2^30 units: on to the pool's alignment
+    assert kvl.kvl_slice_layer(g, fake, least, fake, 1, 2, fake) == kvl.KVL_EINVAL
+    assert kvl.kvl_slice_layer(g, fake, least, fake, 1, 1, fake + 4) == kvl.KVL_EALIGN
+
+
 def test_request_packing_follows_layouts():
     import workloads
     spec = workloads.custom_spec(L=3, P=2, B=4, Rp=32, t_hit=[10, 0], t_miss=[3, 5],
