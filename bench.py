@@ -976,7 +976,9 @@ class EndToEnd:
 
     def link_rates(self, reps=2):
         """The copy engines' rates on this machine for the step's own transfers: inputs in
-        alone, objects out alone (as the step reads them back), and both at once."""
+        alone, objects out alone (as the step reads them back), and both at once, each
+        timed as whole-buffer copies and as the step's per-part copies; the faster of
+        the two counts."""
         import torch
         b = self.bs.bufs
 
@@ -997,20 +999,29 @@ class EndToEnd:
                 best = t if best is None else min(best, t)
             return best
 
-        def up():
+        whole = [dict(hit=(0, b["hit"].numel()), miss=(0, b["miss"].numel()),
+                      obj=(0, self.d_obj[0].numel()))]
+
+        def up(parts):
             with torch.cuda.stream(self.h2d):
                 b["tables"].copy_(self.h_tab, non_blocking=True)
-                b["hit"].copy_(self.t_hit, non_blocking=True)
-                b["miss"].copy_(self.t_miss, non_blocking=True)
+                for part in parts:
+                    (h0, h1), (m0, m1) = part["hit"], part["miss"]
+                    b["hit"][h0:h1].copy_(self.t_hit[h0:h1], non_blocking=True)
+                    b["miss"][m0:m1].copy_(self.t_miss[m0:m1], non_blocking=True)
 
-        def down():
+        def down(parts):
             with torch.cuda.stream(self.d2h):
                 for k in range(self.reads_back):
-                    self.t_obj[k % len(self.t_obj)].copy_(self.d_obj[k % self.ring],
-                                                          non_blocking=True)
+                    for part in parts:
+                        o0, o1 = part["obj"]
+                        self.t_obj[k % len(self.t_obj)][o0:o1].copy_(
+                            self.d_obj[k % self.ring][o0:o1], non_blocking=True)
 
-        t_up, t_down = timed(up), timed(down)
-        t_both = timed(lambda: (up(), down()))
+        pats = [whole] + ([self.parts] if len(self.parts) > 1 else [])
+        t_up = min(timed(lambda: up(p)) for p in pats)
+        t_down = min(timed(lambda: down(p)) for p in pats)
+        t_both = min(timed(lambda: (up(p), down(p))) for p in pats)
         return {"h2d_gbs": round(self.h2d_bytes / t_up / 1e9, 1),
                 "d2h_gbs": round(self.d2h_bytes / t_down / 1e9, 1),
                 "both_gbs": round((self.h2d_bytes + self.d2h_bytes) / t_both / 1e9, 1),
