@@ -58,6 +58,30 @@ MUTATIONS = {
         "memcpy(obj, pool_slot(g, (uint8_t *)pool, 0, p, b, 0), (size_t)obj_bytes);"),
     "scatter_uses_block_index_not_table": (
         "int64_t b = tables[tab0 + t / g->B];", "int64_t b = (tab0 + t / g->B) % g->n_pool;"),
+    "gather_object_layer_term_dropped": (
+        "uint8_t *obj = q->objects + (int64_t)layer * q->obj_layer_stride",
+        "uint8_t *obj = q->objects + 0 * q->obj_layer_stride"),
+    "gather_copies_one_row_of_a_block": (
+        "memcpy(obj, pool_slot(g, (uint8_t *)pool, layer, p, b, 0), (size_t)obj_bytes);",
+        "memcpy(obj, pool_slot(g, (uint8_t *)pool, layer, p, b, 0), (size_t)g->Rp);"),
+    "scatter_back_object_layer_term_dropped": (
+        "const uint8_t *obj = q->objects + (int64_t)layer * q->obj_layer_stride",
+        "const uint8_t *obj = q->objects + 0 * q->obj_layer_stride"),
+    "scatter_back_object_plane_term_dropped": (
+        "const uint8_t *obj = q->objects + (int64_t)layer * q->obj_layer_stride\n"
+        "                                   + (int64_t)p * q->obj_plane_stride",
+        "const uint8_t *obj = q->objects + (int64_t)layer * q->obj_layer_stride\n"
+        "                                   + 0 * q->obj_plane_stride"),
+    "scatter_back_writes_layer_zero": (
+        "memcpy(pool_slot(g, pool, layer, p, b, 0), obj, (size_t)obj_bytes);",
+        "memcpy(pool_slot(g, pool, 0, p, b, 0), obj, (size_t)obj_bytes);"),
+    "scatter_back_ignores_request_table_offset": (
+        "                int64_t b = tables[tab0 + j];\n"
+        "                if (b < 0 || b >= g->n_pool) { note(&status, OR_ERANGE); continue; }\n"
+        "                const uint8_t",
+        "                int64_t b = tables[j];\n"
+        "                if (b < 0 || b >= g->n_pool) { note(&status, OR_ERANGE); continue; }\n"
+        "                const uint8_t"),
 }
 
 PIN_CALLS = [
