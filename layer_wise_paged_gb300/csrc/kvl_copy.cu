@@ -42,8 +42,8 @@
 // before it exits, so it still completes after its predecessor.  With a plan the
 // caller declared complete (KVL_LAUNCH_PLAN_READY), a waiting kernel checks the plan,
 // reads its first records, acquires its first tensor maps, prefetches its first
-// source rows into L2 (cp.async.bulk.prefetch) and decodes its first unit's addresses
-// before the wait.
+// source rows into L2 (cp.async.bulk.prefetch), and works out its segment geometry and
+// its first unit's addresses before the wait.
 #include <cstdint>
 
 #include "kvl_internal.cuh"
@@ -460,14 +460,17 @@ __device__ __forceinline__ bool item_meta(const CopyArgs &a, PlanHeader *h, cons
     return true;
 }
 
-// grid_dependency_wait with the fields of `m` the first copies use as operands, so
-// that they are computed before the wait rather than after it.
-__device__ __forceinline__ void grid_dependency_wait_after(const ItemMeta &m)
+// grid_dependency_wait with the fields of `m` and the segment geometry the first
+// copies use as operands, so that they are computed before the wait rather than
+// after it.
+__device__ __forceinline__ void grid_dependency_wait_after(const ItemMeta &m, int max_rows,
+                                                           int box_rows, int tail_rows,
+                                                           int plane_chunks)
 {
 #if KVL_PDL
     asm volatile("griddepcontrol.wait;" ::"l"(m.src_a), "l"(m.src_b), "l"(m.dst), "l"(m.map_a),
                  "l"(m.a_stride), "l"(m.dst_pstride), "r"(m.n_valid), "r"(m.n_a), "r"(m.tok_a),
-                 "r"(m.blk_a)
+                 "r"(m.blk_a), "r"(max_rows), "r"(box_rows), "r"(tail_rows), "r"(plane_chunks)
                  : "memory");
 #endif
 }
@@ -575,12 +578,22 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
     int64_t n_items = 0, n_hit_all = 0, n_tok_all = 0;
     int32_t map_chunk = 0;
     constexpr bool kMaps = HOST == 0 && (OP == OP_SLICE || OP == OP_MERGE);
+    // Segment geometry, from the call's arguments (and, for the tensor maps' chunks,
+    // the header): worked out before the dependency wait when the plan is complete.
+    const int planes = OP == OP_SLICE ? 1 : a.P;
+    const int row_bytes = OP == OP_SLICE ? a.P * a.Rp : a.Rp;
+    const int max_rows = kStageBytes / row_bytes;  // >= 1 (host-checked)
+    const int64_t R = int64_t(a.P) * a.Rp;
+    const int box_rows = segment_rows(a.B, row_bytes);        // a whole segment's box
+    const int tail_rows = segment_tail_rows(a.B, row_bytes);  // a block tail's box (0: none)
+    int32_t plane_chunks = 0;
     auto read_header = [&]() {
         v = plan_view(a.plan, h->n_req, h->pool_blocks, h->n_layers);
         n_items = h->n_items;
         n_hit_all = h->n_hit;
         n_tok_all = h->n_tokens;
         map_chunk = kMaps ? h->map_chunk : 0;
+        plane_chunks = map_chunk > 0 ? a.Rp / map_chunk : 0;
     };
     // lane 0's four most recently acquired maps, newest first
     const uint8_t *acq0 = nullptr, *acq1 = nullptr, *acq2 = nullptr, *acq3 = nullptr;
@@ -635,7 +648,7 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
                 m_first_ready = true;
             }
         }
-        grid_dependency_wait_after(m_first);
+        grid_dependency_wait_after(m_first, max_rows, box_rows, tail_rows, plane_chunks);
         allow_dependents_launch();
     }
     usable = usable && h->status == KVL_OK;
@@ -649,16 +662,9 @@ __device__ __forceinline__ void copy_rows(const CopyArgs &a)
     ClaimCounter *ctr = &v.counters[int64_t(a.layer) * kOps + OP];
     const int64_t G = gridDim.x;
 
-    const int planes = OP == OP_SLICE ? 1 : a.P;
-    const int row_bytes = OP == OP_SLICE ? a.P * a.Rp : a.Rp;
-    const int max_rows = kStageBytes / row_bytes;  // >= 1 (host-checked)
-    const int64_t R = int64_t(a.P) * a.Rp;
     // Tensor maps (device buffers only): a segment of box_rows rows from one source
     // that has a map is one tensor load; plane p starts at chunk p * Rp / chunk.
     const uint8_t *maps = map_chunk > 0 ? v.maps : nullptr;
-    const int box_rows = segment_rows(a.B, row_bytes);        // a whole segment's box
-    const int tail_rows = segment_tail_rows(a.B, row_bytes);  // a block tail's box (0: none)
-    const int32_t plane_chunks = map_chunk > 0 ? a.Rp / map_chunk : 0;
 
     int64_t issued = 0, retired = 0;
     bool timed_out = false;
