@@ -500,7 +500,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+            "scaling": "strong", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
             "config": dict(describe(spec), us_per_layer=round(dt / args.steps / n * 1e6, 1),
                            layers_per_s=round(args.steps * n / dt, 3)),
             "cpu_baseline": {"value": round(v, 3), "unit": UNIT, "cores": n, "kind": "oracle",

@@ -132,6 +132,8 @@ def test_reference_arm_prints_one_json_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == bench.UNIT and d["metric"] == bench.METRIC
     assert d["value"] > 0 and d["higher_is_better"] is True
+    # the same scaling label as the GPU arm: the total work does not grow with N
+    assert d["scaling"] == "strong"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": bench.UNIT, "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
