@@ -67,8 +67,10 @@
  * launched.  Problems only the device can see (negative counts, misaligned request
  * fields, block ids out of range, duplicate block ids) are recorded in the plan's
  * status word: the offending work is skipped, nothing traps, and every later call
- * made with that plan does nothing until the plan is rebuilt.  kvl_read_status reads
- * the word back.  KVL_ECUDA reports a failed launch.
+ * made with that plan does nothing until the plan is rebuilt.  Of the call that meets
+ * the problem, any part of its other work may be left undone (its CTAs stop once they
+ * see the status).  kvl_read_status reads the word back.  KVL_ECUDA reports a failed
+ * launch.
  */
 #ifndef KVL_H
 #define KVL_H
